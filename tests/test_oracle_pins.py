@@ -1,0 +1,397 @@
+"""Pins for the oracle: checks against things other than the oracle itself.
+
+Each test ties one oracle function to a fact the DLRM pages or plain
+mathematics fix: hand-worked examples (tests/golden/), term counts, a
+textbook matrix product (numpy), the factorization-machine identity, central
+finite differences, brute force over tiny inputs, and library sorts.  A
+plausible slip in the oracle (a dropped term, a wrong sign or index, a
+transposed operand, a missing factor of two, an unstable sort) fails at least
+one of them.
+"""
+import collections
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_dense_interaction_gb300 import workloads as W
+from tests import _golden
+
+
+def _csr(bags_per_table):
+    """Table-major CSR from a list (per table) of lists (per bag) of rows."""
+    T = len(bags_per_table)
+    B = len(bags_per_table[0])
+    offsets = [0]
+    indices = []
+    for t in range(T):
+        for b in range(B):
+            indices.extend(bags_per_table[t][b])
+            offsets.append(len(indices))
+    return np.array(offsets, dtype=np.int64), np.array(indices, dtype=np.int64)
+
+
+def _random_bags(rng, T, B, rows, max_len, dup=True):
+    bags = []
+    for t in range(T):
+        tb = []
+        for _ in range(B):
+            L = int(rng.integers(0, max_len + 1))
+            if dup:
+                tb.append(list(rng.integers(0, rows[t], L)))
+            else:
+                tb.append(list(rng.choice(rows[t], size=min(L, rows[t]), replace=False)))
+        bags.append(tb)
+    return bags
+
+
+def _bf16_bits_to_f64(bits):
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- lookup ---
+
+def test_emb_bag_worked_example():
+    g = _golden.load("emb_bag_worked_example.txt")
+    tables = [g["table0"].reshape(3, 2).astype(np.float32), g["table1"].reshape(2, 2).astype(np.float32)]
+    pooled, mag = oracle.emb_bag_fwd(tables, "f32", g["offsets"], g["indices"], 2)
+    np.testing.assert_array_equal(pooled.reshape(-1), g["pooled"])
+    np.testing.assert_array_equal(mag.reshape(-1), np.abs(g["pooled"]))  # all values positive
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_pooling_factor_one_is_row_copy(dtype):
+    cfg = W.make_config("tiny", dtype=dtype, rows=[50, 70, 30], B=40)
+    tables = W.tables_host(cfg)
+    offsets, indices = W.make_indices(cfg)
+    pooled, _ = oracle.emb_bag_fwd(tables, dtype, offsets, indices, cfg["B"])
+    for t in range(cfg["T"]):
+        idx = indices[offsets[t * cfg["B"]]:offsets[(t + 1) * cfg["B"]]]
+        if dtype == "bf16":
+            expect = _bf16_bits_to_f64(tables[t][idx])
+        else:
+            expect = tables[t][idx].astype(np.float64)  # numpy's own float16 decode
+        np.testing.assert_array_equal(pooled[:, t, :], expect)
+
+
+def test_binary16_decode_covers_all_patterns():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.decode(bits, "f16")
+    ref = bits.view(np.float16).astype(np.float64)
+    finite = np.isfinite(ref)
+    np.testing.assert_array_equal(ours[finite], ref[finite])
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    np.testing.assert_array_equal(np.isinf(ours), np.isinf(ref))
+
+
+@pytest.mark.parametrize("dup", [False, True])
+def test_pooled_equals_bruteforce_sum(dup):
+    rng = np.random.default_rng(1)
+    rows = [40, 9, 77]
+    tables = [rng.standard_normal((r, 5)).astype(np.float32) for r in rows]
+    bags = _random_bags(rng, 3, 16, rows, 8, dup=dup)
+    offsets, indices = _csr(bags)
+    pooled, mag = oracle.emb_bag_fwd(tables, "f32", offsets, indices, 16)
+    for t in range(3):
+        for b in range(16):
+            r = np.array(bags[t][b], dtype=np.int64)
+            got = tables[t][r].astype(np.float64)
+            expect = got.sum(axis=0) if r.size else np.zeros(5)
+            np.testing.assert_allclose(pooled[b, t], expect, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(mag[b, t], np.abs(got).sum(axis=0) if r.size else 0,
+                                       rtol=0, atol=1e-12)
+            assert np.all(mag[b, t] >= np.abs(pooled[b, t]))
+
+
+def test_pooling_is_linear_in_the_bag():
+    rng = np.random.default_rng(2)
+    rows = [25, 31]
+    tables = [rng.standard_normal((r, 6)).astype(np.float32) for r in rows]
+    bags1 = _random_bags(rng, 2, 10, rows, 6)
+    bags2 = _random_bags(rng, 2, 10, rows, 6)
+    union = [[bags1[t][b] + bags2[t][b] for b in range(10)] for t in range(2)]
+    p1, _ = oracle.emb_bag_fwd(tables, "f32", *_csr(bags1), 10)
+    p2, _ = oracle.emb_bag_fwd(tables, "f32", *_csr(bags2), 10)
+    pu, _ = oracle.emb_bag_fwd(tables, "f32", *_csr(union), 10)
+    np.testing.assert_allclose(pu, p1 + p2, rtol=0, atol=1e-12)
+
+
+def test_empty_bags_pool_to_zero():
+    tables = [np.ones((4, 3), dtype=np.float32)]
+    offsets = np.array([0, 0, 0, 2], dtype=np.int64)
+    pooled, _ = oracle.emb_bag_fwd(tables, "f32", offsets, np.array([1, 3]), 3)
+    np.testing.assert_array_equal(pooled[0], 0)
+    np.testing.assert_array_equal(pooled[1], 0)
+    np.testing.assert_array_equal(pooled[2, 0], 2)
+
+
+def test_lookup_errors_are_reported():
+    tables = [np.ones((4, 3), dtype=np.float32)]
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.emb_bag_fwd(tables, "f32", np.array([0, 1]), np.array([4]), 1)
+    assert e.value.status == oracle.INDEX_OOB
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.emb_bag_fwd(tables, "f32", np.array([0, 2, 1]), np.array([0, 1]), 2)
+    assert e.value.status == oracle.BAD_OFFSETS
+
+
+# ----------------------------------------------------------- interaction ---
+
+def test_pair_counts_match_the_pages():
+    for N, inc, d, P, width in _golden.rows("pair_counts.txt"):
+        assert oracle.num_pairs(N, bool(inc)) == P
+        rng = np.random.default_rng(N)
+        y, _ = oracle.interact_fwd(rng.standard_normal((2, d)), rng.standard_normal((2, N, d)),
+                                   bool(inc))
+        assert y.shape == (2, width)
+
+
+@pytest.mark.parametrize("mode", ["strict", "inclusive"])
+def test_interaction_worked_example(mode):
+    g = _golden.load("interaction_worked_example.txt")
+    e0 = g["e0"].reshape(1, 2)
+    emb = g["emb"].reshape(1, 2, 2)
+    y, _ = oracle.interact_fwd(e0, emb, mode == "inclusive")
+    np.testing.assert_array_equal(y[0], g[f"y_{mode}"])
+    de0, _, demb, _ = oracle.interact_bwd(e0, emb, g[f"dy_{mode}"].reshape(1, -1),
+                                          mode == "inclusive")
+    np.testing.assert_array_equal(de0[0], g[f"de0_{mode}"])
+    np.testing.assert_array_equal(demb.reshape(-1), g[f"demb_{mode}"])
+
+
+def _stack(e0, emb):
+    return np.concatenate([e0[:, None, :], emb], axis=1)
+
+
+@pytest.mark.parametrize("inc", [False, True])
+def test_interaction_is_the_triangle_of_a_symmetric_gram_matrix(inc):
+    rng = np.random.default_rng(3)
+    B, N, d = 5, 7, 9
+    e0 = rng.standard_normal((B, d))
+    emb = rng.standard_normal((B, N, d))
+    y, mag = oracle.interact_fwd(e0, emb, inc)
+    Z = _stack(e0, emb)
+    gram = Z @ np.swapaxes(Z, 1, 2)  # textbook matrix product
+    np.testing.assert_allclose(gram, np.swapaxes(gram, 1, 2), rtol=0, atol=1e-12)
+    rr, cc = np.tril_indices(N + 1, k=0 if inc else -1)  # row-major lower triangle
+    np.testing.assert_array_equal(y[:, :d], e0)
+    np.testing.assert_allclose(y[:, d:], gram[:, rr, cc], rtol=0, atol=1e-12)
+    absgram = np.abs(Z) @ np.swapaxes(np.abs(Z), 1, 2)
+    np.testing.assert_allclose(mag[:, d:], absgram[:, rr, cc], rtol=1e-14, atol=0)
+
+
+def test_interaction_bruteforce_dots():
+    rng = np.random.default_rng(4)
+    e0 = rng.standard_normal((3, 4))
+    emb = rng.standard_normal((3, 3, 4))
+    y, _ = oracle.interact_fwd(e0, emb, False)
+    for b in range(3):
+        z = [e0[b]] + [emb[b, i] for i in range(3)]
+        expect = [float(np.dot(z[i], z[j])) for i in range(4) for j in range(i)]
+        np.testing.assert_allclose(y[b, 4:], expect, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("inc", [False, True])
+def test_factorization_machine_identity(inc):
+    # sum_{i<j} z_i.z_j = (|sum z|^2 - sum |z_i|^2) / 2; self pairs add sum |z_i|^2
+    rng = np.random.default_rng(5)
+    e0 = rng.standard_normal((6, 11))
+    emb = rng.standard_normal((6, 12, 11))
+    y, _ = oracle.interact_fwd(e0, emb, inc)
+    Z = _stack(e0, emb)
+    total = (Z.sum(axis=1) ** 2).sum(axis=1)
+    squares = (Z ** 2).sum(axis=(1, 2))
+    expect = 0.5 * (total + squares) if inc else 0.5 * (total - squares)
+    np.testing.assert_allclose(y[:, 11:].sum(axis=1), expect, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("inc", [False, True])
+def test_interaction_backward_by_finite_differences(inc):
+    # L = sum(w * Y) is quadratic in the inputs, so central differences are
+    # exact up to rounding.
+    rng = np.random.default_rng(6)
+    B, N, d = 2, 4, 3
+    e0 = rng.standard_normal((B, d))
+    emb = rng.standard_normal((B, N, d))
+    width = d + oracle.num_pairs(N, inc)
+    w = rng.standard_normal((B, width))
+    de0, _, demb, _ = oracle.interact_bwd(e0, emb, w, inc)
+
+    def loss(a, b):
+        y, _ = oracle.interact_fwd(a, b, inc)
+        return float((w * y).sum())
+
+    h = 1e-3
+    for idx in np.ndindex(e0.shape):
+        p, m = e0.copy(), e0.copy()
+        p[idx] += h
+        m[idx] -= h
+        fd = (loss(p, emb) - loss(m, emb)) / (2 * h)
+        assert abs(fd - de0[idx]) <= 1e-6 * max(1.0, abs(fd))
+    for idx in np.ndindex(emb.shape):
+        p, m = emb.copy(), emb.copy()
+        p[idx] += h
+        m[idx] -= h
+        fd = (loss(e0, p) - loss(e0, m)) / (2 * h)
+        assert abs(fd - demb[idx]) <= 1e-6 * max(1.0, abs(fd))
+
+
+@pytest.mark.parametrize("inc", [False, True])
+def test_interaction_backward_closed_form(inc):
+    # dZ = (G + G^T) Z with G the lower-triangular matrix of upstream gradients
+    rng = np.random.default_rng(7)
+    B, N, d = 4, 6, 5
+    e0 = rng.standard_normal((B, d))
+    emb = rng.standard_normal((B, N, d))
+    F = N + 1
+    dy = rng.standard_normal((B, d + oracle.num_pairs(N, inc)))
+    de0, _, demb, _ = oracle.interact_bwd(e0, emb, dy, inc)
+    rr, cc = np.tril_indices(F, k=0 if inc else -1)
+    G = np.zeros((B, F, F))
+    G[:, rr, cc] = dy[:, d:]
+    dZ = (G + np.swapaxes(G, 1, 2)) @ _stack(e0, emb)
+    np.testing.assert_allclose(de0, dy[:, :d] + dZ[:, 0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(demb, dZ[:, 1:], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ coalescing ---
+
+def test_coalesce_worked_example():
+    g = _golden.load("emb_bag_worked_example.txt")
+    co = oracle.coalesce([3, 2], g["offsets"], g["indices"], 2)
+    for key in ("sorted_pos", "sorted_row", "uniq_table", "uniq_row", "seg_off"):
+        np.testing.assert_array_equal(co[key], g[key])
+    assert co["U"] == 4
+
+
+@pytest.mark.parametrize("kind", ["zipf", "uniform"])
+def test_coalesce_matches_a_library_stable_sort(kind):
+    cfg = W.make_config("multi-hot", rows=[500, 37, 4000, 1], B=64,
+                        index=("zipf", 1.2) if kind == "zipf" else ("uniform",))
+    offsets, indices = W.make_indices(cfg)
+    co = oracle.coalesce(cfg["rows"], offsets, indices, cfg["B"])
+    B = cfg["B"]
+    table_of = np.repeat(np.arange(cfg["T"]), np.diff(offsets[::B]))
+    order = np.lexsort((indices, table_of))  # numpy's lexsort is stable
+    np.testing.assert_array_equal(co["sorted_pos"], order)
+    np.testing.assert_array_equal(co["sorted_row"], indices[order])
+    pairs = sorted(set(zip(table_of.tolist(), indices.tolist())))
+    assert co["U"] == len(pairs)
+    np.testing.assert_array_equal(co["uniq_table"], [p[0] for p in pairs])
+    np.testing.assert_array_equal(co["uniq_row"], [p[1] for p in pairs])
+    counts = collections.Counter(zip(table_of.tolist(), indices.tolist()))
+    np.testing.assert_array_equal(np.diff(co["seg_off"]), [counts[p] for p in pairs])
+    assert co["seg_off"][-1] == indices.size
+
+
+def test_coalesce_properties_with_heavy_duplicates():
+    rng = np.random.default_rng(8)
+    bags = [[list(rng.integers(0, 3, 9)) for _ in range(20)] for _ in range(3)]
+    offsets, indices = _csr(bags)
+    co = oracle.coalesce([3, 3, 3], offsets, indices, 20)
+    sp = co["sorted_pos"]
+    assert sorted(sp.tolist()) == list(range(indices.size))  # a permutation
+    for u in range(co["U"]):
+        seg = sp[co["seg_off"][u]:co["seg_off"][u + 1]]
+        assert np.all(np.diff(seg) > 0)  # ties keep their original order
+        assert np.all(indices[seg] == co["uniq_row"][u])
+
+
+# -------------------------------------------------------- backward + SGD ---
+
+def test_sgd_worked_example():
+    g = _golden.load("emb_bag_worked_example.txt")
+    tables = [g["table0"].reshape(3, 2).astype(np.float32), g["table1"].reshape(2, 2).astype(np.float32)]
+    co = oracle.coalesce([3, 2], g["offsets"], g["indices"], 2)
+    grad, _, new_row, _ = oracle.sgd(tables, "f32", g["offsets"], 2, 6,
+                                     g["dpooled"].reshape(2, 2, 2), float(g["lr"][0]), co)
+    np.testing.assert_array_equal(grad.reshape(-1), g["grad"])
+    np.testing.assert_array_equal(new_row.reshape(-1), g["new_row"])
+
+
+def test_all_duplicate_bag_gives_k_times_the_gradient():
+    k = 13
+    tables = [np.zeros((5, 4), dtype=np.float32)]
+    offsets = np.array([0, k], dtype=np.int64)
+    indices = np.full(k, 3, dtype=np.int64)
+    dp = np.array([[[0.25, -1.5, 3.0, 0.125]]])
+    co = oracle.coalesce([5], offsets, indices, 1)
+    grad, _, new_row, _ = oracle.sgd(tables, "f32", offsets, 1, k, dp, 0.5, co)
+    assert co["U"] == 1 and co["uniq_row"][0] == 3
+    np.testing.assert_array_equal(grad[0], k * dp[0, 0])
+    np.testing.assert_array_equal(new_row[0], -0.5 * k * dp[0, 0])
+
+
+def test_duplicate_updates_equal_the_summed_gradient():
+    rng = np.random.default_rng(9)
+    rows = [6, 11, 4]
+    T, B, d = 3, 12, 3
+    tables = [rng.standard_normal((r, d)).astype(np.float32) for r in rows]
+    bags = _random_bags(rng, T, B, rows, 7)
+    offsets, indices = _csr(bags)
+    dp = rng.standard_normal((B, T, d))
+    co = oracle.coalesce(rows, offsets, indices, B)
+    grad, _, new_row, _ = oracle.sgd(tables, "f32", offsets, B, indices.size, dp, 0.1, co)
+    brute = collections.defaultdict(lambda: np.zeros(d))
+    for t in range(T):
+        for b in range(B):
+            for r in bags[t][b]:
+                brute[(t, int(r))] += dp[b, t]
+    assert co["U"] == len(brute)
+    for u in range(co["U"]):
+        key = (int(co["uniq_table"][u]), int(co["uniq_row"][u]))
+        np.testing.assert_allclose(grad[u], brute[key], rtol=0, atol=1e-12)
+        w = tables[key[0]][key[1]].astype(np.float64)
+        np.testing.assert_allclose(new_row[u], w - 0.1 * brute[key], rtol=0, atol=1e-12)
+
+
+def test_row_gradient_by_finite_differences():
+    # L(W) = sum_{b,t} w_bt . pooled_bt(W) is linear in W; with dyadic table
+    # values and step, the central difference is exact.
+    rng = np.random.default_rng(10)
+    rows = [7, 5]
+    T, B, d = 2, 6, 3
+    tables = [(rng.integers(-64, 64, (r, d)) / 64).astype(np.float32) for r in rows]
+    bags = _random_bags(rng, T, B, rows, 5)
+    offsets, indices = _csr(bags)
+    w = (rng.integers(-8, 8, (B, T, d)) / 8).astype(np.float64)
+    co = oracle.coalesce(rows, offsets, indices, B)
+    grad, _, _, _ = oracle.sgd(tables, "f32", offsets, B, indices.size, w, 0.0, co)
+
+    def loss(tabs):
+        pooled, _ = oracle.emb_bag_fwd(tabs, "f32", offsets, indices, B)
+        return float((w * pooled).sum())
+
+    h = np.float32(1 / 64)
+    for u in range(co["U"]):
+        t, r = int(co["uniq_table"][u]), int(co["uniq_row"][u])
+        for e in range(d):
+            p = [x.copy() for x in tables]
+            m = [x.copy() for x in tables]
+            p[t][r, e] += h
+            m[t][r, e] -= h
+            fd = (loss(p) - loss(m)) / (2 * float(h))
+            assert fd == pytest.approx(grad[u, e], abs=1e-12)
+    # rows that no lookup touches have zero gradient and are not reported
+    touched = set(zip(co["uniq_table"].tolist(), co["uniq_row"].tolist()))
+    for t in range(T):
+        for r in range(rows[t]):
+            if (t, r) not in touched:
+                p = [x.copy() for x in tables]
+                p[t][r, 0] += h
+                assert loss(p) == loss(tables)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_sgd_reads_half_tables_exactly(dtype):
+    cfg = W.make_config("tiny", dtype=dtype, rows=[30, 20], B=16)
+    tables = W.tables_host(cfg)
+    offsets, indices = W.make_indices(cfg)
+    dp = W.make_dpooled(cfg).astype(np.float64)
+    co = oracle.coalesce(cfg["rows"], offsets, indices, cfg["B"])
+    grad, _, new_row, _ = oracle.sgd(tables, dtype, offsets, cfg["B"], indices.size, dp, 0.01, co)
+    for u in range(co["U"]):
+        t, r = int(co["uniq_table"][u]), int(co["uniq_row"][u])
+        wrow = (_bf16_bits_to_f64(tables[t][r]) if dtype == "bf16"
+                else tables[t][r].astype(np.float64))
+        np.testing.assert_allclose(new_row[u], wrow - 0.01 * grad[u], rtol=0, atol=1e-15)
