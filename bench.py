@@ -1,0 +1,523 @@
+#!/usr/bin/env python
+"""Benchmark of the DLRM sparse hot path on one or more GPUs (one JSON line).
+
+A step is one pass of the whole path over one batch of the workload:
+embedding-bag forward -> interaction forward -> interaction backward ->
+embedding-bag backward with row-wise SGD (for a workload without interaction,
+forward -> backward with a resident pooled gradient).  The default workload is
+"multi-hot": 26 fp16 tables x 4M rows x d = 128, batch 65536, Poisson(20) bag
+lengths, Zipf(1.2) indices, strict pairs -- the one configuration that runs
+all of the path's steps at a size that is not launch-bound.
+
+Timing: W warm-up steps, then K steps between two CUDA events on the launch
+stream, with a barrier and a device synchronize on both sides; the max over
+ranks is reported.  Inputs are larger than L2 (tables of tens of GB, indices
+of hundreds of MB per step), so no L2 flush is inserted.  Every kernel of the
+timed steps is also bracketed by CUDA events (recorded on the launch stream
+through the library's profiling hook) to time the dominant kernel for the
+roofline.  SM clocks and throttle reasons are sampled with nvidia-smi during
+the timed region.
+
+``--impl reference`` times the CPU oracle (plain fp64 loops, one core) on a
+bounded sample of the same workload instead.
+
+Multi-GPU: replicas only.  The path's one exchange step (the all-to-all of
+pooled vectors between model-parallel table shards) is not part of this
+build, so N ranks run N independent replicas (weak scaling), one per GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_dense_interaction_gb300 import workloads as W  # noqa: E402
+
+METRIC = "emb-bag+interaction fwd/bwd/SGD samples/s; gathered GB/s as % of HBM peak"
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="multi-hot", choices=sorted(W.CONFIG_IDS))
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ the oracle ---
+
+def oracle_sample(cfg, offsets, indices, Bs, seed):
+    """A bounded sample of the workload for the CPU oracle: the first Bs
+    samples of the batch, each table restricted to the rows those samples
+    look up (renumbered in increasing order, so every result is unchanged)."""
+    T, B, d = cfg["T"], cfg["B"], cfg["d"]
+    sub_off = [np.zeros(1, dtype=np.int64)]
+    sub_idx, tables, rows = [], [], []
+    run = 0
+    for t in range(T):
+        lo, hi = int(offsets[t * B]), int(offsets[t * B + Bs])
+        idx = indices[lo:hi]
+        uniq, inv = np.unique(idx, return_inverse=True)
+        if uniq.size == 0:
+            uniq = np.zeros(1, dtype=np.int64)
+        tables.append(W.table_rows_host(cfg, t, uniq, seed))
+        rows.append(int(uniq.size))
+        sub_idx.append(inv.astype(np.int64))
+        sub_off.append(offsets[t * B + 1:t * B + Bs + 1] - lo + run)
+        run += hi - lo
+    sub = W.make_config(cfg["name"], B=Bs, rows=rows)
+    sub["T"] = T
+    return dict(cfg=sub, tables=tables, offsets=np.concatenate(sub_off),
+                indices=np.concatenate(sub_idx) if sub_idx else np.zeros(0, np.int64),
+                e0=W.make_e0(cfg, seed)[:Bs], dy=W.make_dy(cfg, seed)[:Bs],
+                dpooled=W.make_dpooled(cfg, seed)[:Bs])
+
+
+def oracle_step(s):
+    import oracle
+    cfg = s["cfg"]
+    B, dt = cfg["B"], cfg["dtype"]
+    pooled, pmag = oracle.emb_bag_fwd(s["tables"], dt, s["offsets"], s["indices"], B)
+    if cfg["interaction"]:
+        oracle.interact_fwd(s["e0"], pooled, cfg["include_self"], emb_mag=pmag)
+        _, _, dp, dpm = oracle.interact_bwd(s["e0"], pooled, s["dy"], cfg["include_self"], emb_mag=pmag)
+    else:
+        dp, dpm = s["dpooled"], None
+    co = oracle.coalesce(cfg["rows"], s["offsets"], s["indices"], B)
+    oracle.sgd(s["tables"], dt, s["offsets"], B, s["indices"].size, dp, cfg["lr"], co, dpooled_mag=dpm)
+
+
+def calibrate_oracle(cfg, offsets, indices, seed, seconds):
+    """Picks a sample size whose oracle step takes about `seconds`."""
+    probe = min(128, cfg["B"])
+    s = oracle_sample(cfg, offsets, indices, probe, seed)
+    oracle_step(s)  # first call loads the library and warms the caches
+    t0 = time.perf_counter()
+    oracle_step(s)
+    per_sample = (time.perf_counter() - t0) / probe
+    return int(max(probe, min(cfg["B"], seconds / max(per_sample, 1e-9))))
+
+
+def cpu_baseline(cfg, offsets, indices, seed, seconds):
+    import oracle
+    oracle.build()
+    Bs = calibrate_oracle(cfg, offsets, indices, seed, seconds)
+    s = oracle_sample(cfg, offsets, indices, Bs, seed)
+    t0 = time.perf_counter()
+    oracle_step(s)
+    el = time.perf_counter() - t0
+    return {"value": Bs / el, "unit": "samples/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {Bs} of {cfg['B']} samples of the same batch (all {cfg['T']} tables, "
+                      f"{s['indices'].size} lookups), full step in fp64 on one host core, {el:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cfg = W.make_config(args.workload)
+    offsets, indices = W.make_indices(cfg, args.seed)
+    budget = 90.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    Bs = calibrate_oracle(cfg, offsets, indices, args.seed, min(3.0, budget))
+    s = oracle_sample(cfg, offsets, indices, Bs, args.seed)
+    for _ in range(args.warmup):
+        oracle_step(s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(s)
+    el = time.perf_counter() - t0
+    value = Bs * args.steps / el
+    sample = (f"first {Bs} of {cfg['B']} samples of the batch per step (all {cfg['T']} tables, "
+              f"{s['indices'].size} lookups), fp64 oracle on one host core")
+    print(json.dumps({
+        "metric": METRIC, "value": value, "unit": "samples/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(cfg),
+        "cpu_baseline": {"value": value, "unit": "samples/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def config_of(cfg):
+    return {"workload": cfg["name"], "tables": cfg["T"], "rows_per_table": cfg["rows"][0]
+            if len(set(cfg["rows"])) == 1 else f"{min(cfg['rows'])}..{max(cfg['rows'])}",
+            "d": cfg["d"], "table_dtype": cfg["dtype"], "global_batch": cfg["B"],
+            "bag": "x".join(str(v) for v in cfg["bag"]), "index": "x".join(str(v) for v in cfg["index"]),
+            "pairs": ("self-inclusive" if cfg["include_self"] else "strict") if cfg["interaction"] else "none",
+            "update": cfg["update"], "lr": cfg["lr"], "parallelism": "replicas",
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+# --------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                smax.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.file.name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ the GPU run ---
+
+class Step:
+    """Device buffers and the launches of one step of the path."""
+
+    def __init__(self, cfg, seed, dev):
+        import torch
+
+        import sparse_dense_interaction_gb300 as sdi
+        self.sdi, self.torch, self.cfg, self.dev = sdi, torch, cfg, dev
+        B, T, d = cfg["B"], cfg["T"], cfg["d"]
+        self.offsets_h, self.indices_h = W.make_indices(cfg, seed)
+        self.nnz = int(self.indices_h.size)
+        self.tables = W.make_tables_device(cfg, seed, dev)
+        self.offsets = torch.from_numpy(self.offsets_h).to(dev)
+        self.indices = torch.from_numpy(self.indices_h).to(dev)
+        self.inter = cfg["interaction"]
+        self.P = sdi.dlrm_num_pairs(T, cfg["include_self"]) if self.inter else 0
+        self.pooled = torch.empty((B, T, d), device=dev)
+        self.dpooled = torch.empty((B, T, d), device=dev)
+        if self.inter:
+            self.e0 = torch.from_numpy(W.make_e0(cfg, seed)).to(dev)
+            self.dy = torch.from_numpy(W.make_dy(cfg, seed)).to(dev)
+            self.y = torch.empty((B, d + self.P), device=dev)
+            self.de0 = torch.empty((B, d), device=dev)
+        else:
+            self.dpooled.copy_(torch.from_numpy(W.make_dpooled(cfg, seed)))
+        self.ws = torch.empty(sdi.dlrm_emb_bag_bwd_workspace_size(T, B, self.nnz, d), dtype=torch.uint8,
+                              device=dev)
+        self.grad = torch.empty((self.nnz, d), device=dev) if cfg["update"] == "grad" else None
+        self.flag = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(self, prof=None):
+        """One step; with `prof`, a list that receives (kernel name, start event, end event)."""
+        sdi, c = self.sdi, self.cfg
+        calls = [("emb_bag_fwd", lambda: sdi.dlrm_emb_bag_fwd(self.tables, self.offsets, self.indices,
+                                                                c["B"], self.pooled, err_flag=self.flag))]
+        if self.inter:
+            calls.append(("interact_fwd", lambda: sdi.dlrm_interact_fwd(self.e0, self.pooled,
+                                                                        c["include_self"], self.y)))
+            calls.append(("interact_bwd", lambda: sdi.dlrm_interact_bwd(
+                self.e0, self.pooled, c["include_self"], self.dy, self.de0, self.dpooled)))
+        calls.append(("emb_bag_bwd", lambda: sdi.dlrm_emb_bag_bwd_sgd(
+            self.tables, self.offsets, self.indices, c["B"], self.dpooled, c["lr"], self.ws,
+            grad_rows=self.grad, err_flag=self.flag)))
+        for name, fn in calls:
+            if prof is None:
+                fn()
+            else:
+                prof.begin(name)
+                fn()
+                prof.end()
+
+
+class KernelProfiler:
+    """Brackets every library kernel of the timed steps with CUDA events."""
+
+    BWD_NAMES = None
+
+    def __init__(self, torch, sdi, stream, n_steps, max_per_call=24):
+        self.torch, self.sdi, self.stream = torch, sdi, stream
+        self.pool = []
+        self.calls = []  # (call name, start event, [events after each kernel])
+        n = n_steps * 4
+        for _ in range(n):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(max_per_call + 1)]
+            for e in evs:
+                e.record(stream)  # creates the CUDA handle
+            self.pool.append(evs)
+        torch.cuda.synchronize()
+        self.next = 0
+        self.cur = None
+
+    def begin(self, name):
+        evs = self.pool[self.next]
+        self.next += 1
+        evs[0].record(self.stream)
+        self.sdi.dlrm_profile_events(evs[1:])
+        self.cur = (name, evs, self.sdi.dlrm_kernel_launch_count())
+
+    def end(self):
+        name, evs, before = self.cur
+        self.sdi.dlrm_profile_events([])
+        n = self.sdi.dlrm_kernel_launch_count() - before
+        self.calls.append((name, evs, n))
+
+    def per_kernel_ms(self):
+        """{(call, kernel index): [ms per launch]} over all recorded steps."""
+        out = {}
+        for name, evs, n in self.calls:
+            for k in range(n):
+                out.setdefault((name, k), []).append(evs[k].elapsed_time(evs[k + 1]))
+        return out
+
+
+BWD_KERNELS_PREFIX = ["bwd_prep", "bag_ids"]
+
+
+def bwd_kernel_names(passes):
+    names = list(BWD_KERNELS_PREFIX)
+    for p in range(passes):
+        names += [f"sort_upsweep[{p}]", f"sort_scan[{p}]", f"sort_downsweep[{p}]"]
+    return names + ["seg_count", "seg_scan", "seg_reduce", "seg_finalize"]
+
+
+def algorithmic_bytes(cfg, st):
+    """Compulsory HBM bytes of each single-kernel call per launch (each
+    distinct table row counted once; streams read or written once)."""
+    B, T, d = cfg["B"], cfg["T"], cfg["d"]
+    es = W.ELEM_BYTES[cfg["dtype"]]
+    nb = T * B
+    uniq = 0
+    for t in range(T):
+        lo, hi = st.offsets_h[t * B], st.offsets_h[(t + 1) * B]
+        uniq += np.unique(st.indices_h[lo:hi]).size
+    out = {
+        "emb_bag_fwd": st.nnz * 8 + (nb + 1) * 8 + uniq * d * es + nb * d * 4,
+    }
+    if st.inter:
+        width = d + st.P
+        out["interact_fwd"] = B * (T + 1) * d * 4 + B * width * 4
+        out["interact_bwd"] = B * (T + 1) * d * 4 + B * width * 4 + B * (T + 1) * d * 4
+    # the reduce + update kernel: sorted keys and positions, bag ids, the
+    # pooled gradient, and one read-modify-write of every unique row
+    out["seg_reduce"] = st.nnz * 12 + nb * d * 4 + 2 * uniq * d * es
+    return out, uniq
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_dense_interaction_gb300 as sdi
+    from sparse_dense_interaction_gb300 import build as cuda_build
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        cuda_build.build()
+    if world > 1:
+        dist.barrier()
+    sdi.load()
+
+    cfg = W.make_config(args.workload)
+    st = Step(cfg, args.seed + rank, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+    status = sdi.dlrm_read_error(st.flag)
+    if status != 0:
+        raise RuntimeError(f"device error flag after warm-up: {sdi.status_string(status)}")
+
+    # timed region: K steps between two events, kernels bracketed by events
+    prof = KernelProfiler(torch, sdi, stream, args.steps)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = sdi.dlrm_kernel_launch_count()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        st.run(prof)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = sdi.dlrm_kernel_launch_count() - launches0
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.steps
+    value = cfg["B"] * world / (ms_step / 1e3)
+
+    # per-kernel times (events on the launch stream) and the roofline
+    per = prof.per_kernel_ms()
+    bits = max(1, int(np.ceil(np.log2(max(cfg["rows"])))))
+    passes = (bits + 7) // 8
+    names = {}
+    for (call, k) in per:
+        names[(call, k)] = bwd_kernel_names(passes)[k] if call == "emb_bag_bwd" else call
+    kernel_ms = {names[key]: float(np.mean(v)) for key, v in per.items()}
+    alg, uniq = algorithmic_bytes(cfg, st)
+    peak, peak_kind = measured_peaks()
+    dominant = max(kernel_ms, key=kernel_ms.get)
+    rl_kernel = dominant if dominant in alg else max((k for k in kernel_ms if k in alg), key=kernel_ms.get)
+    achieved = alg[rl_kernel] / (kernel_ms[rl_kernel] / 1e3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(cfg["name"], {}).get(rl_kernel)
+    roofline = {"kernel": rl_kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "algorithmic_bytes": alg[rl_kernel], "peak_source": peak_kind,
+                "kernel_ms": kernel_ms[rl_kernel]}
+    es = W.ELEM_BYTES[cfg["dtype"]]
+    gathered = st.nnz * cfg["d"] * es / (kernel_ms["emb_bag_fwd"] / 1e3) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = e2e_measure(args, st, torch, sdi, stream, dev)
+
+    status = sdi.dlrm_read_error(st.flag)
+    if status != 0:
+        raise RuntimeError(f"device error flag after timing: {sdi.status_string(status)}")
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(cfg, st.offsets_h, st.indices_h, args.seed, args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 accumulate, " + cfg["dtype"] + " tables",
+            "data": "synthetic (seeded; Zipf/uniform indices, counter-hash tables)",
+            "config": config_of(cfg),
+            "gathered": {"gbs": gathered, "frac_of_hbm_peak": gathered / peak,
+                         "bytes": st.nnz * cfg["d"] * es, "unique_rows": uniq, "lookups": st.nnz},
+            "roofline": roofline,
+            "kernels_ms": kernel_ms,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "cpu_baseline": base,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def e2e_measure(args, st, torch, sdi, stream, dev):
+    """Same metric through the public API, inputs from pinned host memory and
+    the step's results read back every step."""
+    c = st.cfg
+    K = args.e2e_steps or max(3, args.steps // 2)
+    h_off = torch.from_numpy(st.offsets_h).pin_memory()
+    h_idx = torch.from_numpy(st.indices_h).pin_memory()
+    ins = [(h_off, st.offsets), (h_idx, st.indices)]
+    outs = []
+    if st.inter:
+        ins += [(st.e0.cpu().pin_memory(), st.e0), (st.dy.cpu().pin_memory(), st.dy)]
+        outs += [(st.y, torch.empty(st.y.shape, pin_memory=True)),
+                 (st.de0, torch.empty(st.de0.shape, pin_memory=True))]
+    else:
+        ins += [(st.dpooled.cpu().pin_memory(), st.dpooled)]
+        outs += [(st.pooled, torch.empty(st.pooled.shape, pin_memory=True))]
+    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
+    d2h = sum(h.numel() * h.element_size() for _, h in outs)
+
+    def once():
+        for h, d_ in ins:
+            d_.copy_(h, non_blocking=True)
+        st.run()
+        for d_, h in outs:
+            h.copy_(d_, non_blocking=True)
+
+    once()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        once()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / K
+    return {"value": c["B"] / (ms / 1e3), "unit": "samples/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * dlrm_sparse.h -- C ABI of the GB300 (sm_103a) DLRM sparse hot path.
+ *
+ * The path, as the Deep Learning Recommendation Model is described in
+ * "Notes/DLRM" (vault-aram.pages.dev) and in "Terabyte Embedding Tables and
+ * Compute-Bound Neural Layers Force Meta's DLRM to Split Training"
+ * (factlen.com):
+ *   1. embedding-bag forward   (sum-pooled lookups, one table per feature)
+ *   2. interaction forward     (pairwise dot products, concatenated with e0)
+ *   3. interaction backward
+ *   4. embedding-bag backward  (coalescing of duplicate rows + row-wise SGD)
+ *
+ * Conventions shared by every call:
+ *  - Tensor pointers are DEVICE pointers owned by the caller unless a
+ *    parameter says "host".  The library never allocates device memory;
+ *    scratch space comes from a caller-provided workspace.
+ *  - Every compute call is asynchronous on the given stream (a cudaStream_t
+ *    passed as void*; NULL is the legacy default stream) and never
+ *    synchronizes with the host.
+ *  - Host-detectable errors (bad sizes, null pointers, misalignment the call
+ *    cannot handle, short workspace) are returned synchronously before
+ *    anything is launched.  Data-dependent errors (an index outside its
+ *    table, inconsistent offsets) are raised as bits in an optional device
+ *    int32 flag; the offending lookup is skipped (it contributes zero), no
+ *    kernel faults or traps.  Read the flag with dlrm_read_error().
+ *  - Lookups are table-major CSR: bag (t, b) of table t and sample b is
+ *    indices[offsets[t*B + b] .. offsets[t*B + b + 1]), offsets has T*B + 1
+ *    int64 entries with offsets[0] == 0 and offsets[T*B] == nnz, indices has
+ *    nnz int64 row numbers.
+ *  - Tables are row-major [rows_t][d] in fp32, fp16 or bf16; pooled values,
+ *    interaction values and all gradients are fp32; all accumulation is fp32.
+ *  - Return value: DLRM_OK (0) or a negative dlrm_status.
+ */
+#ifndef DLRM_SPARSE_H
+#define DLRM_SPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *dlrm_stream_t; /* a cudaStream_t */
+
+enum dlrm_dtype { DLRM_F32 = 0, DLRM_F16 = 1, DLRM_BF16 = 2 };
+
+enum dlrm_status {
+    DLRM_OK = 0,
+    DLRM_ERR_INVALID_ARG = -1,
+    DLRM_ERR_UNSUPPORTED = -2,
+    DLRM_ERR_WORKSPACE_TOO_SMALL = -3,
+    DLRM_ERR_INDEX_OOB = -4,
+    DLRM_ERR_BAD_OFFSETS = -5,
+    DLRM_ERR_CAPACITY = -6,
+    DLRM_ERR_CUDA = -7
+};
+
+/* Bits of the device error flag. */
+#define DLRM_FLAG_INDEX_OOB 1   /* an index was < 0 or >= rows of its table */
+#define DLRM_FLAG_BAD_OFFSETS 2 /* offsets not monotone, or not 0 .. nnz */
+#define DLRM_FLAG_CAPACITY 4    /* more unique rows than grad_rows can hold */
+
+#define DLRM_MAX_TABLES 256
+
+/*
+ * Embedding-bag forward ("Notes/DLRM", section 2: one embedding table per
+ * categorical feature, each ID looked up as a learned vector; section 9:
+ * multi-valued features are aggregated -- here by summation).
+ *
+ *   out[b*out_sample_stride + t*out_table_stride + e]
+ *       = sum_{k in bag (t,b)} tables[t][indices[k]*d + e]      (fp32 sum)
+ *
+ * tables    host array of T device pointers, each 16-byte aligned for the
+ *           vectorised path (any alignment of the element size works).
+ * rows      host array of T row counts (1 .. 2^32-2).
+ * T, d      number of tables (1 .. DLRM_MAX_TABLES), embedding dimension.
+ * dtype     storage type of all tables (dlrm_dtype).
+ * offsets   device int64 [T*B + 1];  indices  device int64 [nnz].
+ * out       device fp32, strides in elements; with out_table_stride = d and
+ *           out_sample_stride = T*d it is the [B][T][d] pooled block.
+ * err_flag  optional device int32 (NULL: no flag); bits are OR-ed in.
+ * An empty bag pools to zero.  An out-of-range index contributes zero and
+ * sets DLRM_FLAG_INDEX_OOB; a bag with bad offsets pools to zero and sets
+ * DLRM_FLAG_BAD_OFFSETS.
+ */
+int dlrm_emb_bag_fwd(const void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                     const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                     float *out, int64_t out_sample_stride, int64_t out_table_stride,
+                     int32_t *err_flag, dlrm_stream_t stream);
+
+/*
+ * Number of interaction terms over F = N + 1 vectors (e0 and N pooled
+ * embeddings): F(F-1)/2 strict pairs, F(F+1)/2 with self pairs
+ * ("Notes/DLRM", section 3; N(N+1)/2 there counts the strict pairs of
+ * e0..eN).  Returns -1 if N < 0.
+ */
+int64_t dlrm_num_pairs(int N, int include_self);
+
+/*
+ * Interaction forward ("Notes/DLRM", section 3, and the architecture figure
+ * of section 2).  With z_0 = e0[b] and z_i = emb[b][i-1] (i = 1..N):
+ *
+ *   y[b][0 .. d)      = e0[b]                    (the concatenated e0)
+ *   y[b][d + p(i,j)]  = z_i . z_j   for j < i (strict) or j <= i (self pairs)
+ *   p(i,j)            = i(i-1)/2 + j (strict),  i(i+1)/2 + j (self pairs)
+ *
+ * e0    device fp32 rows of d, row stride e0_stride (elements).
+ * emb   device fp32; pooled embedding i of sample b at
+ *       emb[b*emb_sample_stride + i*d] (the [B][N][d] block of
+ *       dlrm_emb_bag_fwd with out_table_stride = d).
+ * y     device fp32 rows of d + dlrm_num_pairs(N, include_self), row stride
+ *       y_stride.  N may be 0 .. 127.
+ */
+int dlrm_interact_fwd(const float *e0, int64_t e0_stride, const float *emb,
+                      int64_t emb_sample_stride, int N, int d, int64_t B, int include_self,
+                      float *y, int64_t y_stride, dlrm_stream_t stream);
+
+/*
+ * Interaction backward: the gradient of the forward above by the product
+ * rule.  With G the F x F matrix holding dy[b][d + p(i,j)] at (i, j), j <= i,
+ * and zero above the diagonal:
+ *
+ *   dZ        = (G + G^T) Z        (a self term contributes 2 g_ii z_i)
+ *   de0[b]    = dy[b][0 .. d) + dZ[0]
+ *   demb[b*demb_sample_stride + (i-1)*d + e] = dZ[i][e]     (i = 1..N)
+ *
+ * Inputs as in dlrm_interact_fwd; dy has row stride dy_stride, de0 row
+ * stride de0_stride.  Outputs are overwritten (not accumulated).
+ */
+int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb,
+                      int64_t emb_sample_stride, int N, int d, int64_t B, int include_self,
+                      const float *dy, int64_t dy_stride, float *de0, int64_t de0_stride,
+                      float *demb, int64_t demb_sample_stride, dlrm_stream_t stream);
+
+/*
+ * Device pointers into the workspace of the last dlrm_emb_bag_bwd_sgd call,
+ * valid once the stream has passed that call and until the workspace is
+ * reused.  The coalescing is a stable sort of lookup positions by
+ * (table, row) followed by run-length encoding; U = *num_unique.
+ */
+typedef struct dlrm_coalesced_view {
+    const uint32_t *sorted_pos; /* [nnz] positions k, sorted; ties keep position order */
+    const uint32_t *sorted_row; /* [nnz] indices[sorted_pos[j]] */
+    const int32_t *uniq_table;  /* [U] table of each unique key, ascending */
+    const uint32_t *uniq_row;   /* [U] row of each unique key, ascending within a table */
+    const uint32_t *seg_off;    /* [U + 1] first sorted position of each key; [U] = nnz */
+    const int64_t *num_unique;  /* [1] U */
+} dlrm_coalesced_view;
+
+/*
+ * Bytes of workspace dlrm_emb_bag_bwd_sgd needs for these sizes (a bound
+ * that does not depend on the data).  Returns 0 for invalid sizes.
+ */
+size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d);
+
+/*
+ * Embedding-bag backward with row-wise SGD ("Notes/DLRM", section 5: the
+ * tables are trained by an optimizer; plain SGD on the touched rows here).
+ * Duplicate lookups are coalesced first (stable radix sort by (table, row),
+ * run-length encoding), then for every unique key u = (t, r):
+ *
+ *   g_u = sum over the lookups k of r in table t, in sorted order, of
+ *         dpooled[b(k)*dp_sample_stride + t*dp_table_stride + 0 .. d)
+ *   tables[t][r] <- tables[t][r] - lr * g_u     (fp32; one rounding to the
+ *                                                table type, nearest even)
+ *
+ * Rows no lookup touches are not written.  lr == 0 leaves the tables
+ * untouched (the coalesced gradient only).
+ * grad_rows      optional device fp32 [grad_rows_cap][d]: receives g_u in
+ *                row u; if U > grad_rows_cap the rows past the cap are not
+ *                written and DLRM_FLAG_CAPACITY is raised.
+ * workspace      device memory of at least
+ *                dlrm_emb_bag_bwd_workspace_size(T, B, nnz, d) bytes,
+ *                256-byte aligned; its content need not be initialised.
+ * view           optional host struct, filled with device pointers to the
+ *                integer results of the coalescing (see above).
+ * nnz may be at most 2^31 and B at most 2^31 - 1 (DLRM_ERR_UNSUPPORTED
+ * beyond); B == 0 requires nnz == 0.  The vectorised path needs d % 4 == 0,
+ * 16-byte aligned tables, dpooled and grad_rows, and dpooled strides that are
+ * multiples of 4; other layouts take a scalar path.
+ */
+int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                         const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                         const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride,
+                         float lr, float *grad_rows, int64_t grad_rows_cap, void *workspace,
+                         size_t workspace_bytes, dlrm_coalesced_view *view, int32_t *err_flag,
+                         dlrm_stream_t stream);
+
+/* Synchronizes the stream, reads the flag and maps its bits to a status
+ * (DLRM_OK if no bit is set).  A CUDA failure returns DLRM_ERR_CUDA. */
+int dlrm_read_error(const int32_t *err_flag, dlrm_stream_t stream);
+
+/* Clears the flag asynchronously on the stream. */
+int dlrm_clear_error(int32_t *err_flag, dlrm_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *dlrm_status_string(int status);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t dlrm_kernel_launch_count(void);
+
+/*
+ * Profiling aid (the pages have no counterpart): registers n cudaEvent_t
+ * handles (passed as void*) for the calling host thread.  After each of the
+ * next n kernel launches the library makes on this thread, it records the
+ * next event on that launch's stream, so a caller can time every kernel of a
+ * multi-kernel call with events of its own.  n = 0 unregisters.  The events
+ * stay owned by the caller; at most DLRM_MAX_PROFILE_EVENTS.
+ */
+#define DLRM_MAX_PROFILE_EVENTS 64
+int dlrm_profile_events(void *const *events, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLRM_SPARSE_H */

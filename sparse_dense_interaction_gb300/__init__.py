@@ -1,0 +1,13 @@
+"""GB300 (sm_103a) DLRM sparse hot path.
+
+The path -- embedding-bag forward, pairwise-interaction forward and backward,
+embedding-bag backward with row-wise SGD -- runs in the CUDA library
+``libdlrm_sparse.so`` behind the C ABI of ``include/dlrm_sparse.h``.  This
+package is its thin Python binding (same names, torch tensors in, argument
+marshalling only) plus the seeded workload generator used by the tests and
+the benchmark.
+"""
+from ._native import (  # noqa: F401
+    BF16, F16, F32, MAX_TABLES, DlrmError, dlrm_clear_error, dlrm_emb_bag_bwd_sgd,
+    dlrm_emb_bag_bwd_workspace_size, dlrm_emb_bag_fwd, dlrm_interact_bwd, dlrm_interact_fwd,
+    dlrm_kernel_launch_count, dlrm_num_pairs, dlrm_profile_events, dlrm_read_error, library_path, load, status_string)

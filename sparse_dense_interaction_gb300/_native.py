@@ -1,0 +1,217 @@
+"""ctypes binding of ``libdlrm_sparse.so`` (C ABI: ``include/dlrm_sparse.h``).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  The functions carry the C names and take torch CUDA tensors (torch
+provides device memory and streams); they raise :class:`DlrmError` on a
+non-zero status.  There is no fallback: if the library is missing the first
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+F32, F16, BF16 = 0, 1, 2
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL = 0, -1, -2, -3
+ERR_INDEX_OOB, ERR_BAD_OFFSETS, ERR_CAPACITY, ERR_CUDA = -4, -5, -6, -7
+FLAG_INDEX_OOB, FLAG_BAD_OFFSETS, FLAG_CAPACITY = 1, 2, 4
+MAX_TABLES = 256
+
+_TORCH_DTYPES = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+# (name, restype, argtypes) of every exported entry point
+_i32, _i64, _u64, _vp, _sz, _f32 = (ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p,
+                                    ctypes.c_size_t, ctypes.c_float)
+
+
+class CoalescedView(ctypes.Structure):
+    _fields_ = [("sorted_pos", _vp), ("sorted_row", _vp), ("uniq_table", _vp),
+                ("uniq_row", _vp), ("seg_off", _vp), ("num_unique", _vp)]
+
+
+SIGNATURES = {
+    "dlrm_emb_bag_fwd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64, _i64,
+                                _vp, _vp]),
+    "dlrm_num_pairs": (_i64, [_i32, _i32]),
+    "dlrm_interact_fwd": (_i32, [_vp, _i64, _vp, _i64, _i32, _i32, _i64, _i32, _vp, _i64, _vp]),
+    "dlrm_interact_bwd": (_i32, [_vp, _i64, _vp, _i64, _i32, _i32, _i64, _i32, _vp, _i64, _vp,
+                                 _i64, _vp, _i64, _vp]),
+    "dlrm_emb_bag_bwd_workspace_size": (_sz, [_i32, _i64, _i64, _i32]),
+    "dlrm_emb_bag_bwd_sgd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64,
+                                    _i64, _f32, _vp, _i64, _vp, _sz, ctypes.POINTER(CoalescedView),
+                                    _vp, _vp]),
+    "dlrm_read_error": (_i32, [_vp, _vp]),
+    "dlrm_clear_error": (_i32, [_vp, _vp]),
+    "dlrm_status_string": (ctypes.c_char_p, [_i32]),
+    "dlrm_kernel_launch_count": (_u64, []),
+    "dlrm_profile_events": (_i32, [_vp, _i32]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DlrmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.lib_path("libdlrm_sparse.so")
+
+
+def load():
+    """Loads the CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it first "
+                                   "(python -m sparse_dense_interaction_gb300.build)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().dlrm_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise DlrmError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _tables(tables):
+    T = len(tables)
+    ptrs = (ctypes.c_void_p * max(T, 1))(*[t.data_ptr() for t in tables])
+    rows = (ctypes.c_int64 * max(T, 1))(*[t.shape[0] for t in tables])
+    dtype = _TORCH_DTYPES[tables[0].dtype]
+    for t in tables:
+        if t.dtype != tables[0].dtype or t.dim() != 2 or t.stride(1) != 1 or t.stride(0) != t.shape[1]:
+            raise ValueError("tables must share one dtype and be contiguous [rows][d]")
+    return ptrs, rows, T, tables[0].shape[1], dtype
+
+
+def dlrm_emb_bag_fwd(tables, offsets, indices, B: int, out, err_flag=None, stream=None):
+    """Sum-pooled lookups into ``out`` ([B][T][d] fp32, any strides, last dim 1)."""
+    ptrs, rows, T, d, dtype = _tables(tables)
+    if out.stride(2) != 1:
+        raise ValueError("out must have unit stride in its last dimension")
+    _check(load().dlrm_emb_bag_fwd(ptrs, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices),
+                                   indices.numel(), B, out.data_ptr(), out.stride(0), out.stride(1),
+                                   _ptr(err_flag), _stream(stream)), "dlrm_emb_bag_fwd")
+
+
+def dlrm_num_pairs(N: int, include_self: bool) -> int:
+    return int(load().dlrm_num_pairs(N, int(bool(include_self))))
+
+
+def dlrm_interact_fwd(e0, emb, include_self: bool, y, stream=None):
+    """``y[b] = [e0[b] | z_i . z_j over pairs]`` for ``emb`` of shape [B][N][d]."""
+    B, N, d = emb.shape
+    if emb.stride(2) != 1 or emb.stride(1) != d or e0.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("rows must be contiguous and emb's tables adjacent")
+    _check(load().dlrm_interact_fwd(e0.data_ptr(), e0.stride(0), emb.data_ptr(), emb.stride(0), N, d,
+                                    B, int(bool(include_self)), y.data_ptr(), y.stride(0),
+                                    _stream(stream)), "dlrm_interact_fwd")
+
+
+def dlrm_interact_bwd(e0, emb, include_self: bool, dy, de0, demb, stream=None):
+    """Gradients of :func:`dlrm_interact_fwd` into ``de0`` [B][d] and ``demb`` [B][N][d]."""
+    B, N, d = emb.shape
+    for t in (emb, demb):
+        if t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError("rows must be contiguous and tables adjacent")
+    _check(load().dlrm_interact_bwd(e0.data_ptr(), e0.stride(0), emb.data_ptr(), emb.stride(0), N, d,
+                                    B, int(bool(include_self)), dy.data_ptr(), dy.stride(0),
+                                    de0.data_ptr(), de0.stride(0), demb.data_ptr(), demb.stride(0),
+                                    _stream(stream)), "dlrm_interact_bwd")
+
+
+def dlrm_emb_bag_bwd_workspace_size(T: int, B: int, nnz: int, d: int) -> int:
+    return int(load().dlrm_emb_bag_bwd_workspace_size(T, B, nnz, d))
+
+
+def dlrm_emb_bag_bwd_sgd(tables, offsets, indices, B: int, dpooled, lr: float, workspace,
+                         grad_rows=None, err_flag=None, stream=None, want_view: bool = False):
+    """Coalesces duplicate lookups and applies row-wise SGD to ``tables`` in place.
+
+    ``dpooled`` is [B][T][d] fp32 (any strides, last dim 1); ``workspace`` a
+    uint8 CUDA tensor of at least :func:`dlrm_emb_bag_bwd_workspace_size`
+    bytes; ``grad_rows`` an optional [cap][d] fp32 tensor for the coalesced
+    gradients.  With ``want_view`` returns a dict of tensor views into the
+    workspace (sorted_pos, sorted_row, uniq_table, uniq_row, seg_off as
+    uint32/int32 of capacity nnz or nnz + 1, and num_unique as int64[1]).
+    """
+    ptrs, rows, T, d, dtype = _tables(tables)
+    if dpooled.stride(2) != 1:
+        raise ValueError("dpooled must have unit stride in its last dimension")
+    view = CoalescedView()
+    nnz = indices.numel()
+    cap = 0 if grad_rows is None else grad_rows.shape[0]
+    _check(load().dlrm_emb_bag_bwd_sgd(ptrs, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices), nnz,
+                                       B, dpooled.data_ptr(), dpooled.stride(0), dpooled.stride(1),
+                                       float(lr), _ptr(grad_rows), cap, workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(),
+                                       ctypes.byref(view) if want_view else None, _ptr(err_flag),
+                                       _stream(stream)), "dlrm_emb_bag_bwd_sgd")
+    if not want_view:
+        return None
+    base = workspace.data_ptr()
+
+    def sub(ptr, n, dt):
+        off = ptr - base
+        return workspace[off:off + n * 4].view(dt) if dt != torch.int64 else workspace[off:off + 8].view(dt)
+
+    return dict(sorted_pos=sub(view.sorted_pos, nnz, torch.int32),
+                sorted_row=sub(view.sorted_row, nnz, torch.int32),
+                uniq_table=sub(view.uniq_table, nnz, torch.int32),
+                uniq_row=sub(view.uniq_row, nnz, torch.int32),
+                seg_off=sub(view.seg_off, nnz + 1, torch.int32),
+                num_unique=sub(view.num_unique, 1, torch.int64))
+
+
+def dlrm_read_error(err_flag, stream=None) -> int:
+    """Synchronizes the stream and returns the status the flag's bits map to."""
+    return int(load().dlrm_read_error(err_flag.data_ptr(), _stream(stream)))
+
+
+def dlrm_clear_error(err_flag, stream=None):
+    _check(load().dlrm_clear_error(err_flag.data_ptr(), _stream(stream)), "dlrm_clear_error")
+
+
+def dlrm_kernel_launch_count() -> int:
+    return int(load().dlrm_kernel_launch_count())
+
+
+def dlrm_profile_events(events):
+    """Registers torch CUDA events to be recorded after each of the library's
+    next kernel launches on this thread (``[]`` unregisters).  Each event must
+    have been recorded once already, so that its CUDA handle exists."""
+    handles = [e.cuda_event for e in events]
+    if any(h == 0 for h in handles):
+        raise ValueError("record each event once before registering it")
+    arr = (ctypes.c_void_p * max(len(handles), 1))(*handles)
+    _check(load().dlrm_profile_events(arr, len(handles)), "dlrm_profile_events")

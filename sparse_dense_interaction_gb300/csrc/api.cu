@@ -1,0 +1,276 @@
+// C ABI of the DLRM sparse path: argument checks and dispatch.
+//
+// Every check here runs on the host before anything is launched, so a call
+// with bad sizes or pointers returns an error without touching the GPU.
+#include <atomic>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace dlrm {
+
+static std::atomic<uint64_t> g_launches{0};
+
+// Profiling events registered by the calling host thread.
+static thread_local cudaEvent_t g_prof_events[DLRM_MAX_PROFILE_EVENTS];
+static thread_local int g_prof_n = 0, g_prof_next = 0;
+
+void count_launch(cudaStream_t st)
+{
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (g_prof_next < g_prof_n)
+        cudaEventRecord(g_prof_events[g_prof_next++], st);
+}
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA; }
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
+
+// kernels (defined in the other translation units)
+bool emb_bag_fwd_vectorisable(const TableSet &, int, int, int, const float *, int64_t, int64_t);
+int launch_emb_bag_fwd(const TableSet &, int, int, int, bool, const int64_t *, const int64_t *, int64_t,
+                       int64_t, float *, int64_t, int64_t, int32_t *, cudaStream_t);
+int launch_interact_fwd(const float *, int64_t, const float *, int64_t, int, int, int64_t, int, float *,
+                        int64_t, cudaStream_t);
+int launch_interact_bwd(const float *, int64_t, const float *, int64_t, int, int, int64_t, int,
+                        const float *, int64_t, float *, int64_t, float *, int64_t, cudaStream_t);
+bool emb_bag_bwd_vectorisable(const TableSet &, int, int, const float *, int64_t, int64_t, const float *);
+size_t emb_bag_bwd_workspace(int, int64_t, int);
+int launch_emb_bag_bwd(const TableSet &, int, int, int, const int64_t *, const int64_t *, int64_t, int64_t,
+                       const float *, int64_t, int64_t, float, float *, int64_t, void *, bool,
+                       dlrm_coalesced_view *, int32_t *, cudaStream_t);
+
+// Lookup positions are 32-bit in the backward's sort and scans; the bound
+// leaves headroom for tile and chunk arithmetic.
+static const int64_t kMaxLookups = (int64_t)1 << 31;
+
+static int elem_bytes(int dtype) { return dtype == DLRM_F32 ? 4 : 2; }
+
+static bool aligned(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// Common checks of the table arguments; fills the kernel-parameter view.
+static int make_tables(const void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                       TableSet &ts)
+{
+    if (!tables || !rows || T <= 0 || d <= 0)
+        return DLRM_ERR_INVALID_ARG;
+    if (dtype != DLRM_F32 && dtype != DLRM_F16 && dtype != DLRM_BF16)
+        return DLRM_ERR_INVALID_ARG;
+    if (T > DLRM_MAX_TABLES)
+        return DLRM_ERR_UNSUPPORTED;
+    std::memset(&ts, 0, sizeof ts);
+    for (int t = 0; t < T; t++) {
+        if (!tables[t] || rows[t] <= 0)
+            return DLRM_ERR_INVALID_ARG;
+        if (rows[t] > (int64_t)0xfffffffeLL)
+            return DLRM_ERR_UNSUPPORTED;
+        if (!aligned(tables[t], (size_t)elem_bytes(dtype)))
+            return DLRM_ERR_INVALID_ARG;
+        ts.ptr[t] = tables[t];
+        ts.rows[t] = rows[t];
+    }
+    return DLRM_OK;
+}
+
+}  // namespace dlrm
+
+using namespace dlrm;
+
+extern "C" {
+
+int dlrm_emb_bag_fwd(const void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                     const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                     float *out, int64_t out_sample_stride, int64_t out_table_stride,
+                     int32_t *err_flag, dlrm_stream_t stream)
+{
+    TableSet ts;
+    int s = make_tables(tables, rows, T, d, dtype, ts);
+    if (s != DLRM_OK)
+        return s;
+    if (B < 0 || nnz < 0 || out_sample_stride < 0 || out_table_stride < 0)
+        return DLRM_ERR_INVALID_ARG;
+    if (B == 0)
+        return DLRM_OK;
+    if (!offsets || !out || (nnz > 0 && !indices) || !aligned(out, 4))
+        return DLRM_ERR_INVALID_ARG;
+    if (!aligned(offsets, 8) || (indices && !aligned(indices, 8)))
+        return DLRM_ERR_INVALID_ARG;
+    const bool vec = emb_bag_fwd_vectorisable(ts, T, d, elem_bytes(dtype), out, out_sample_stride,
+                                              out_table_stride);
+    return launch_emb_bag_fwd(ts, T, d, dtype, vec, offsets, indices, nnz, B, out, out_sample_stride,
+                              out_table_stride, err_flag, static_cast<cudaStream_t>(stream));
+}
+
+int64_t dlrm_num_pairs(int N, int include_self)
+{
+    if (N < 0)
+        return -1;
+    const int64_t F = (int64_t)N + 1;
+    return include_self ? F * (F + 1) / 2 : F * (F - 1) / 2;
+}
+
+static int check_interact(const float *e0, int64_t e0_stride, const float *emb, int64_t emb_sample_stride,
+                          int N, int d, int64_t B)
+{
+    if (N < 0 || d <= 0 || B < 0 || e0_stride < d || (N > 0 && emb_sample_stride < (int64_t)N * d))
+        return DLRM_ERR_INVALID_ARG;
+    if (N > 127 || B > (int64_t)1 << 31)
+        return DLRM_ERR_UNSUPPORTED;
+    if (B > 0 && (!e0 || (N > 0 && !emb)))
+        return DLRM_ERR_INVALID_ARG;
+    if (!aligned(e0, 4) || !aligned(emb, 4))
+        return DLRM_ERR_INVALID_ARG;
+    return DLRM_OK;
+}
+
+int dlrm_interact_fwd(const float *e0, int64_t e0_stride, const float *emb, int64_t emb_sample_stride,
+                      int N, int d, int64_t B, int include_self, float *y, int64_t y_stride,
+                      dlrm_stream_t stream)
+{
+    int s = check_interact(e0, e0_stride, emb, emb_sample_stride, N, d, B);
+    if (s != DLRM_OK)
+        return s;
+    if (y_stride < d + dlrm_num_pairs(N, include_self) || (B > 0 && !y) || !aligned(y, 4))
+        return DLRM_ERR_INVALID_ARG;
+    if (B == 0)
+        return DLRM_OK;
+    return launch_interact_fwd(e0, e0_stride, emb, emb_sample_stride, N, d, B, include_self ? 1 : 0, y,
+                               y_stride, static_cast<cudaStream_t>(stream));
+}
+
+int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb, int64_t emb_sample_stride,
+                      int N, int d, int64_t B, int include_self, const float *dy, int64_t dy_stride,
+                      float *de0, int64_t de0_stride, float *demb, int64_t demb_sample_stride,
+                      dlrm_stream_t stream)
+{
+    int s = check_interact(e0, e0_stride, emb, emb_sample_stride, N, d, B);
+    if (s != DLRM_OK)
+        return s;
+    if (dy_stride < d + dlrm_num_pairs(N, include_self) || de0_stride < d ||
+        (N > 0 && demb_sample_stride < (int64_t)N * d))
+        return DLRM_ERR_INVALID_ARG;
+    if (B > 0 && (!dy || !de0 || (N > 0 && !demb)))
+        return DLRM_ERR_INVALID_ARG;
+    if (!aligned(dy, 4) || !aligned(de0, 4) || !aligned(demb, 4))
+        return DLRM_ERR_INVALID_ARG;
+    if (B == 0)
+        return DLRM_OK;
+    return launch_interact_bwd(e0, e0_stride, emb, emb_sample_stride, N, d, B, include_self ? 1 : 0, dy,
+                               dy_stride, de0, de0_stride, demb, demb_sample_stride,
+                               static_cast<cudaStream_t>(stream));
+}
+
+size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d)
+{
+    if (T <= 0 || T > DLRM_MAX_TABLES || B < 0 || nnz < 0 || nnz > kMaxLookups || d <= 0)
+        return 0;
+    return emb_bag_bwd_workspace(T, nnz, d);
+}
+
+int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                         const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                         const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride,
+                         float lr, float *grad_rows, int64_t grad_rows_cap, void *workspace,
+                         size_t workspace_bytes, dlrm_coalesced_view *view, int32_t *err_flag,
+                         dlrm_stream_t stream)
+{
+    TableSet ts;
+    int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
+    if (s != DLRM_OK)
+        return s;
+    if (B < 0 || nnz < 0 || dp_sample_stride < 0 || dp_table_stride < 0 || grad_rows_cap < 0)
+        return DLRM_ERR_INVALID_ARG;
+    if (nnz > kMaxLookups || B > (int64_t)0x7fffffffLL)
+        return DLRM_ERR_UNSUPPORTED;
+    if (B == 0 && nnz != 0)  // no bags cannot hold lookups
+        return DLRM_ERR_INVALID_ARG;
+    if (!(lr == lr))  // NaN learning rate
+        return DLRM_ERR_INVALID_ARG;
+    if (!offsets || !workspace || !aligned(workspace, 256) || !aligned(offsets, 8))
+        return DLRM_ERR_INVALID_ARG;
+    if (nnz > 0 && (!indices || !aligned(indices, 8) || !dpooled || !aligned(dpooled, 4)))
+        return DLRM_ERR_INVALID_ARG;
+    if (grad_rows && !aligned(grad_rows, 4))
+        return DLRM_ERR_INVALID_ARG;
+    if (workspace_bytes < emb_bag_bwd_workspace(T, nnz, d))
+        return DLRM_ERR_WORKSPACE_TOO_SMALL;
+    const bool vec = emb_bag_bwd_vectorisable(ts, T, d, dpooled, dp_sample_stride, dp_table_stride, grad_rows);
+    return launch_emb_bag_bwd(ts, T, d, dtype, offsets, indices, nnz, B, dpooled, dp_sample_stride,
+                              dp_table_stride, lr, grad_rows, grad_rows ? grad_rows_cap : 0, workspace, vec,
+                              view, err_flag, static_cast<cudaStream_t>(stream));
+}
+
+int dlrm_read_error(const int32_t *err_flag, dlrm_stream_t stream)
+{
+    if (!err_flag)
+        return DLRM_ERR_INVALID_ARG;
+    int32_t h = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        cudaMemcpy(&h, err_flag, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    if (h & DLRM_FLAG_INDEX_OOB)
+        return DLRM_ERR_INDEX_OOB;
+    if (h & DLRM_FLAG_BAD_OFFSETS)
+        return DLRM_ERR_BAD_OFFSETS;
+    if (h & DLRM_FLAG_CAPACITY)
+        return DLRM_ERR_CAPACITY;
+    return DLRM_OK;
+}
+
+int dlrm_clear_error(int32_t *err_flag, dlrm_stream_t stream)
+{
+    if (!err_flag)
+        return DLRM_ERR_INVALID_ARG;
+    return cudaMemsetAsync(err_flag, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DLRM_OK
+               : DLRM_ERR_CUDA;
+}
+
+const char *dlrm_status_string(int status)
+{
+    switch (status) {
+    case DLRM_OK:
+        return "ok";
+    case DLRM_ERR_INVALID_ARG:
+        return "invalid argument";
+    case DLRM_ERR_UNSUPPORTED:
+        return "unsupported size or layout";
+    case DLRM_ERR_WORKSPACE_TOO_SMALL:
+        return "workspace too small";
+    case DLRM_ERR_INDEX_OOB:
+        return "index out of range of its table";
+    case DLRM_ERR_BAD_OFFSETS:
+        return "offsets not monotone or not spanning 0..nnz";
+    case DLRM_ERR_CAPACITY:
+        return "more unique rows than grad_rows can hold";
+    case DLRM_ERR_CUDA:
+        return "CUDA error";
+    default:
+        return "unknown status";
+    }
+}
+
+uint64_t dlrm_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int dlrm_profile_events(void *const *events, int n)
+{
+    if (n < 0 || n > DLRM_MAX_PROFILE_EVENTS || (n > 0 && !events))
+        return DLRM_ERR_INVALID_ARG;
+    for (int i = 0; i < n; i++) {
+        if (!events[i])
+            return DLRM_ERR_INVALID_ARG;
+        g_prof_events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    g_prof_n = n;
+    g_prof_next = 0;
+    return DLRM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// Shared device helpers of the sm_103a DLRM sparse path.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dlrm_sparse.h"
+
+namespace dlrm {
+
+// Kernel-parameter view of the caller's tables (4 KB at 256 tables, well
+// inside the 32 KB parameter space of sm_70+ kernels).
+struct TableSet {
+    const void *ptr[DLRM_MAX_TABLES];
+    int64_t rows[DLRM_MAX_TABLES];
+};
+
+// Called after every kernel launch: counts it and, when the calling thread
+// has registered profiling events, records the next one on the stream.
+void count_launch(cudaStream_t st);
+// cudaGetLastError mapped to a status, for use right after a launch.
+int launch_status();
+// Streaming multiprocessor count of the current device.
+int sm_count();
+
+__device__ __forceinline__ void raise_flag(int32_t *flag, int bits)
+{
+    if (flag)
+        atomicOr(flag, bits);
+}
+
+// 16-byte table chunk -> fp32 values.
+template <typename TT>
+struct Chunk16;
+
+template <>
+struct Chunk16<float> {
+    static constexpr int kElems = 4;
+    __device__ __forceinline__ static void add(float *acc, const uint4 &v)
+    {
+        acc[0] += __uint_as_float(v.x);
+        acc[1] += __uint_as_float(v.y);
+        acc[2] += __uint_as_float(v.z);
+        acc[3] += __uint_as_float(v.w);
+    }
+};
+
+template <>
+struct Chunk16<__half> {
+    static constexpr int kElems = 8;
+    __device__ __forceinline__ static void add(float *acc, const uint4 &v)
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 f = __half22float2(h);
+            acc[2 * i] += f.x;
+            acc[2 * i + 1] += f.y;
+        }
+    }
+};
+
+template <>
+struct Chunk16<__nv_bfloat16> {
+    static constexpr int kElems = 8;
+    __device__ __forceinline__ static void add(float *acc, const uint4 &v)
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            // bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 word
+            acc[2 * i] += __uint_as_float(w[i] << 16);
+            acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+template <typename TT>
+__device__ __forceinline__ float to_f32(TT v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename TT>
+__device__ __forceinline__ TT from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// Loads that should not displace hot table rows from L2.
+__device__ __forceinline__ int64_t load_stream(const int64_t *p) { return __ldcs(p); }
+__device__ __forceinline__ uint4 load_table(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+
+}  // namespace dlrm

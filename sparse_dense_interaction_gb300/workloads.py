@@ -26,7 +26,7 @@ Recipe (all seeded; ``seed`` defaults to 0):
   24 bits m give v = (2m - 2^24) * 2^-24 exactly in fp32, the value is
   fp32(v * fp32(1/sqrt(R_t))) rounded once more, to nearest even, into the
   table's storage type.  The same definition runs on the host here (any subset
-  of rows) and on the device in ``csrc/workload_gen.cu`` (whole tables), so a
+  of rows) and on the device in ``workloads_csrc/workload_gen.cu`` (whole tables), so a
   131 GB table set never has to exist on the host;
 * e0, dY and standalone pooled gradients: N(0, 1) in fp32.
 """
@@ -232,3 +232,63 @@ def make_dpooled(cfg: dict, seed: int = 0) -> np.ndarray:
 
 def table_bytes(cfg: dict) -> int:
     return sum(cfg["rows"]) * cfg["d"] * ELEM_BYTES[cfg["dtype"]]
+
+
+_fill_lib = None
+
+
+def _load_fill():
+    global _fill_lib
+    if _fill_lib is None:
+        import ctypes
+        import os
+
+        from . import build as _build
+        path = _build.lib_path("libdlrm_workloads.so")
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first "
+                               "(python -m sparse_dense_interaction_gb300.build)")
+        lib = ctypes.CDLL(path)
+        lib.dlrm_workload_fill_table.restype = ctypes.c_int
+        lib.dlrm_workload_fill_table.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                                 ctypes.c_int, ctypes.c_uint64, ctypes.c_float,
+                                                 ctypes.c_void_p]
+        _fill_lib = lib
+    return _fill_lib
+
+
+_DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def make_tables_device(cfg: dict, seed: int = 0, device="cuda"):
+    """All tables of a configuration, allocated and filled on the GPU.
+
+    Same values as :func:`table_rows_host`, generated by the device copy of
+    the counter-based generator (workload input only).
+    """
+    import torch
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[cfg["dtype"]]
+    lib = _load_fill()
+    stream = torch.cuda.current_stream(device)
+    tables = []
+    for t in range(cfg["T"]):
+        tab = torch.empty((cfg["rows"][t], cfg["d"]), dtype=tdt, device=device)
+        st = lib.dlrm_workload_fill_table(tab.data_ptr(), _DTYPE_CODE[cfg["dtype"]], cfg["rows"][t],
+                                          cfg["d"], table_stream_seed(cfg, t, seed),
+                                          float(table_scale(cfg["rows"][t])), stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"table fill failed with status {st}")
+        tables.append(tab)
+    return tables
+
+
+def tables_to_device(host_tables, dtype: str, device="cuda"):
+    """Uploads host tables (bf16 given as uint16 bit patterns)."""
+    import torch
+    out = []
+    for h in host_tables:
+        if dtype == "bf16":
+            out.append(torch.from_numpy(h.view(np.int16).copy()).to(device).view(torch.bfloat16))
+        else:
+            out.append(torch.from_numpy(np.ascontiguousarray(h)).to(device))
+    return out

@@ -1,0 +1,124 @@
+"""The C-ABI library: it loads, exports what the header declares, and rejects
+bad arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_dense_interaction_gb300 as sdi
+from sparse_dense_interaction_gb300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _native.load()
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(dlrm_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_path(lib):
+    names = declared_functions()
+    for required in ("dlrm_emb_bag_fwd", "dlrm_interact_fwd", "dlrm_interact_bwd",
+                     "dlrm_emb_bag_bwd_sgd", "dlrm_emb_bag_bwd_workspace_size"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _native.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings_and_pair_counts(lib):
+    assert sdi.status_string(0) == "ok"
+    assert "workspace" in sdi.status_string(-3)
+    assert sdi.dlrm_num_pairs(8, False) == 36
+    assert sdi.dlrm_num_pairs(26, False) == 351
+    assert sdi.dlrm_num_pairs(100, True) == 5151
+    assert lib.dlrm_num_pairs(-1, 0) == -1
+
+
+def test_workspace_size_grows_with_the_batch(lib):
+    a = sdi.dlrm_emb_bag_bwd_workspace_size(26, 65536, 1_000_000, 128)
+    b = sdi.dlrm_emb_bag_bwd_workspace_size(26, 65536, 2_000_000, 128)
+    assert 32 * 1_000_000 <= a < b
+    assert sdi.dlrm_emb_bag_bwd_workspace_size(0, 1, 1, 1) == 0
+    assert sdi.dlrm_emb_bag_bwd_workspace_size(1, 1, (1 << 31) + 1, 1) == 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails its host checks first
+
+
+def _tables(n, rows=100):
+    ptrs = (ctypes.c_void_p * n)(*([FAKE] * n))
+    r = (ctypes.c_int64 * n)(*([rows] * n))
+    return ptrs, r
+
+
+def test_forward_rejects_bad_arguments(lib):
+    p, r = _tables(4)
+    call = lambda **kw: lib.dlrm_emb_bag_fwd(
+        kw.get("tables", p), kw.get("rows", r), kw.get("T", 4), kw.get("d", 16), kw.get("dtype", 0),
+        kw.get("offsets", FAKE), FAKE, 10, kw.get("B", 2), kw.get("out", FAKE), 64, 16, None, None)
+    assert call(T=0) == _native.ERR_INVALID_ARG
+    assert call(d=0) == _native.ERR_INVALID_ARG
+    assert call(dtype=3) == _native.ERR_INVALID_ARG
+    assert call(tables=None) == _native.ERR_INVALID_ARG
+    assert call(offsets=None) == _native.ERR_INVALID_ARG
+    assert call(out=None) == _native.ERR_INVALID_ARG
+    assert call(B=-1) == _native.ERR_INVALID_ARG
+    big_p, big_r = _tables(_native.MAX_TABLES + 1)
+    assert call(tables=big_p, rows=big_r, T=_native.MAX_TABLES + 1) == _native.ERR_UNSUPPORTED
+    zero_rows = (ctypes.c_int64 * 4)(100, 0, 100, 100)
+    assert call(rows=zero_rows) == _native.ERR_INVALID_ARG
+    huge_rows = (ctypes.c_int64 * 4)(100, 1 << 33, 100, 100)
+    assert call(rows=huge_rows) == _native.ERR_UNSUPPORTED
+    assert call(B=0) == _native.OK  # nothing to do, nothing launched
+    assert lib.dlrm_kernel_launch_count() == 0
+
+
+def test_interaction_rejects_bad_arguments(lib):
+    fwd = lambda N=4, d=8, B=2, ys=100, y=FAKE: lib.dlrm_interact_fwd(
+        FAKE, d, FAKE, max(N, 1) * d, N, d, B, 0, y, ys, None)
+    assert fwd(N=-1) == _native.ERR_INVALID_ARG
+    assert fwd(d=0) == _native.ERR_INVALID_ARG
+    assert fwd(N=128, ys=10000) == _native.ERR_UNSUPPORTED
+    assert fwd(ys=8 + 10 - 1) == _native.ERR_INVALID_ARG  # width d + P = 18
+    assert fwd(y=None) == _native.ERR_INVALID_ARG
+    assert fwd(B=0) == _native.OK
+    bwd = lambda dys=18, de0s=8: lib.dlrm_interact_bwd(FAKE, 8, FAKE, 32, 4, 8, 2, 0, FAKE, dys, FAKE,
+                                                       de0s, FAKE, 32, None)
+    assert bwd(dys=17) == _native.ERR_INVALID_ARG
+    assert bwd(de0s=7) == _native.ERR_INVALID_ARG
+    assert lib.dlrm_kernel_launch_count() == 0
+
+
+def test_backward_rejects_bad_arguments(lib):
+    p, r = _tables(2)
+    need = sdi.dlrm_emb_bag_bwd_workspace_size(2, 8, 100, 16)
+    call = lambda **kw: lib.dlrm_emb_bag_bwd_sgd(
+        p, r, 2, 16, 0, FAKE, FAKE, kw.get("nnz", 100), 8, FAKE, 32, 16, kw.get("lr", 0.1), None, 0,
+        kw.get("ws", 0x100000), kw.get("ws_bytes", need), None, None, None)
+    assert call(ws_bytes=need - 1) == _native.ERR_WORKSPACE_TOO_SMALL
+    assert call(ws=0x100010) == _native.ERR_INVALID_ARG  # workspace not 256-byte aligned
+    assert call(nnz=(1 << 31) + 1) == _native.ERR_UNSUPPORTED
+    assert call(nnz=-1) == _native.ERR_INVALID_ARG
+    assert call(lr=float("nan")) == _native.ERR_INVALID_ARG
+    assert lib.dlrm_kernel_launch_count() == 0
+
+
+def test_read_error_needs_a_flag(lib):
+    assert lib.dlrm_read_error(None, None) == _native.ERR_INVALID_ARG
+    assert lib.dlrm_clear_error(None, None) == _native.ERR_INVALID_ARG
