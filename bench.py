@@ -57,7 +57,21 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--batch", type=int, default=None, help="override the batch size (profiling runs)")
+    p.add_argument("--tables", type=int, default=None, help="override the table count (profiling runs)")
+    p.add_argument("--rows", type=int, default=None, help="override the rows per table (profiling runs)")
     return p.parse_args()
+
+
+def workload_config(args):
+    over = {}
+    if args.tables is not None:
+        over["T"] = args.tables
+    if args.rows is not None:
+        over["rows"] = [args.rows] * (args.tables or W.make_config(args.workload)["T"])
+    if args.batch is not None:
+        over["B"] = args.batch
+    return W.make_config(args.workload, **over)
 
 
 def measured_peaks():
@@ -142,7 +156,7 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    cfg = W.make_config(args.workload)
+    cfg = workload_config(args)
     offsets, indices = W.make_indices(cfg, args.seed)
     budget = 90.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
     Bs = calibrate_oracle(cfg, offsets, indices, args.seed, min(3.0, budget))
@@ -175,6 +189,20 @@ def config_of(cfg):
             "pairs": ("self-inclusive" if cfg["include_self"] else "strict") if cfg["interaction"] else "none",
             "update": cfg["update"], "lr": cfg["lr"], "parallelism": "replicas",
             "l2": "inputs larger than L2 (no flush)"}
+
+
+def aggregate_over_ranks(ms, units, device=None):
+    """(max elapsed ms, total units) over the ranks of the default process
+    group; the local values when there is no group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms), float(units)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
 
 
 # --------------------------------------------------------------- clocks ---
@@ -377,7 +405,7 @@ def run_ours(args):
         dist.barrier()
     sdi.load()
 
-    cfg = W.make_config(args.workload)
+    cfg = workload_config(args)
     st = Step(cfg, args.seed + rank, dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -407,13 +435,9 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     launches = sdi.dlrm_kernel_launch_count() - launches0
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms, samples = aggregate_over_ranks(t0.elapsed_time(t1), cfg["B"] * args.steps, dev)
     ms_step = ms / args.steps
-    value = cfg["B"] * world / (ms_step / 1e3)
+    value = samples / (ms / 1e3)
 
     # per-kernel times (events on the launch stream) and the roofline
     per = prof.per_kernel_ms()
