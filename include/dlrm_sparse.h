@@ -187,6 +187,37 @@ int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d,
                          size_t workspace_bytes, dlrm_coalesced_view *view, int32_t *err_flag,
                          dlrm_stream_t stream);
 
+/*
+ * dlrm_emb_bag_bwd_sgd for callers that cannot allocate device memory (the
+ * pages have no counterpart to this; it is a deployment aid).  Some callers
+ * can neither call cudaMalloc nor hand the library a workspace -- a plugin
+ * whose host framework passes it only its input and output tensors and owns
+ * every device allocation, or a service that must not touch the device
+ * allocator once it runs.  This variant computes exactly what
+ * dlrm_emb_bag_bwd_sgd computes, with the same arguments minus the workspace,
+ * and allocates nothing: its scratch is a fixed array of
+ * DLRM_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.
+ *  - Sizes whose scratch would not fit (dlrm_emb_bag_bwd_workspace_size(T, B,
+ *    nnz, d) > DLRM_NOALLOC_SCRATCH_BYTES; about 1.8M lookups at d = 128) are
+ *    refused with DLRM_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - The first call on each device looks up the array's device address (a
+ *    CUDA runtime query, made with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the array and it keeps the last call's contents; the
+ *    call re-initialises what it needs.  Calls that may run at the same time
+ *    on the GPU (different streams with no ordering between them) race on it
+ *    and must not be issued.  The view, if requested, points into the array
+ *    and is valid until the next call.
+ */
+#define DLRM_NOALLOC_SCRATCH_BYTES (64 * 1024 * 1024)
+int dlrm_emb_bag_bwd_sgd_noalloc(void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                                 const int64_t *offsets, const int64_t *indices, int64_t nnz,
+                                 int64_t B, const float *dpooled, int64_t dp_sample_stride,
+                                 int64_t dp_table_stride, float lr, float *grad_rows,
+                                 int64_t grad_rows_cap, dlrm_coalesced_view *view,
+                                 int32_t *err_flag, dlrm_stream_t stream);
+
 /* Synchronizes the stream, reads the flag and maps its bits to a status
  * (DLRM_OK if no bit is set).  A CUDA failure returns DLRM_ERR_CUDA. */
 int dlrm_read_error(const int32_t *err_flag, dlrm_stream_t stream);

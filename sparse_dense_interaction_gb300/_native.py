@@ -45,6 +45,9 @@ SIGNATURES = {
     "dlrm_emb_bag_bwd_sgd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64,
                                     _i64, _f32, _vp, _i64, _vp, _sz, ctypes.POINTER(CoalescedView),
                                     _vp, _vp]),
+    "dlrm_emb_bag_bwd_sgd_noalloc": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp,
+                                            _i64, _i64, _f32, _vp, _i64, ctypes.POINTER(CoalescedView),
+                                            _vp, _vp]),
     "dlrm_read_error": (_i32, [_vp, _vp]),
     "dlrm_clear_error": (_i32, [_vp, _vp]),
     "dlrm_status_string": (ctypes.c_char_p, [_i32]),
@@ -191,6 +194,26 @@ def dlrm_emb_bag_bwd_sgd(tables, offsets, indices, B: int, dpooled, lr: float, w
                 uniq_row=sub(view.uniq_row, nnz, torch.int32),
                 seg_off=sub(view.seg_off, nnz + 1, torch.int32),
                 num_unique=sub(view.num_unique, 1, torch.int64))
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def dlrm_emb_bag_bwd_sgd_noalloc(tables, offsets, indices, B: int, dpooled, lr: float,
+                                 grad_rows=None, err_flag=None, stream=None):
+    """:func:`dlrm_emb_bag_bwd_sgd` without a workspace: the library's fixed
+    scratch array is used instead, so nothing is allocated.  For callers that
+    cannot allocate device memory; sizes whose scratch exceeds
+    ``NOALLOC_SCRATCH_BYTES`` raise (status DLRM_ERR_WORKSPACE_TOO_SMALL)."""
+    ptrs, rows, T, d, dtype = _tables(tables)
+    if dpooled.stride(2) != 1:
+        raise ValueError("dpooled must have unit stride in its last dimension")
+    cap = 0 if grad_rows is None else grad_rows.shape[0]
+    _check(load().dlrm_emb_bag_bwd_sgd_noalloc(ptrs, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices),
+                                               indices.numel(), B, dpooled.data_ptr(), dpooled.stride(0),
+                                               dpooled.stride(1), float(lr), _ptr(grad_rows), cap, None,
+                                               _ptr(err_flag), _stream(stream)),
+           "dlrm_emb_bag_bwd_sgd_noalloc")
 
 
 def dlrm_read_error(err_flag, stream=None) -> int:
