@@ -31,50 +31,42 @@ __device__ __forceinline__ void raise_flag(int32_t *flag, int bits)
         atomicOr(flag, bits);
 }
 
-// 16-byte table chunk -> fp32 values.
+// 16-byte table chunk added into fp32 accumulators (kElems/2 float2 pairs),
+// with packed fp32 adds.
 template <typename TT>
 struct Chunk16;
 
 template <>
 struct Chunk16<float> {
     static constexpr int kElems = 4;
-    __device__ __forceinline__ static void add(float *acc, const uint4 &v)
+    __device__ __forceinline__ static void add(float2 *acc, const uint4 &v)
     {
-        acc[0] += __uint_as_float(v.x);
-        acc[1] += __uint_as_float(v.y);
-        acc[2] += __uint_as_float(v.z);
-        acc[3] += __uint_as_float(v.w);
+        acc[0] = __fadd2_rn(acc[0], make_float2(__uint_as_float(v.x), __uint_as_float(v.y)));
+        acc[1] = __fadd2_rn(acc[1], make_float2(__uint_as_float(v.z), __uint_as_float(v.w)));
     }
 };
 
 template <>
 struct Chunk16<__half> {
     static constexpr int kElems = 8;
-    __device__ __forceinline__ static void add(float *acc, const uint4 &v)
+    __device__ __forceinline__ static void add(float2 *acc, const uint4 &v)
     {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
-            float2 f = __half22float2(h);
-            acc[2 * i] += f.x;
-            acc[2 * i + 1] += f.y;
-        }
+        for (int i = 0; i < 4; i++)
+            acc[i] = __fadd2_rn(acc[i], __half22float2(*reinterpret_cast<const __half2 *>(&w[i])));
     }
 };
 
 template <>
 struct Chunk16<__nv_bfloat16> {
     static constexpr int kElems = 8;
-    __device__ __forceinline__ static void add(float *acc, const uint4 &v)
+    __device__ __forceinline__ static void add(float2 *acc, const uint4 &v)
     {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            // bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 word
-            acc[2 * i] += __uint_as_float(w[i] << 16);
-            acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
-        }
+        for (int i = 0; i < 4; i++)  // bf16 -> fp32 is exact: the bf16 bits are the top half of the word
+            acc[i] = __fadd2_rn(acc[i], make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)));
     }
 };
 

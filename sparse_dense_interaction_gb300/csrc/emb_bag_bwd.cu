@@ -15,35 +15,18 @@
 //                tile histograms -> per-(table,digit) scan across tiles ->
 //                stable local ranking in shared memory (warp match + per-warp
 //                histograms) and a coalesced scatter.
-//  4. count      segment starts per 512-position chunk of the sorted order
-//  5. scan       exclusive scan of the per-tile counts: unique ids
-//  6. reduce     one warp per chunk: walks its 512 sorted lookups, gathers
-//                the pooled gradient rows (16-byte loads, 8 rows in flight
-//                per lane), accumulates each run of equal rows in fp32 and
-//                applies SGD to the run's row in place, one read-modify-write
-//                per unique row.  Runs that cross chunk boundaries leave
-//                partial sums.  Work per warp is fixed (512 lookups) however
-//                skewed the row distribution is.
-//  7. finalize   the warp whose chunk holds the start of a crossing run sums
-//                the partials in chunk order and applies the update, so every
-//                result is deterministic.
-#include "common.cuh"
+//  4. count      run starts (a new row, or a table's first lookup) per tile
+//  5. scan       exclusive scan of the per-tile counts: the runs' unique ids
+//  6. reduce     per tile, the summed pooled gradient of every run of equal
+//                rows and the SGD update of its row (seg_reduce.cu)
+//  7. finalize   runs that cross chunk boundaries (seg_reduce.cu)
+#include "emb_bag_bwd.cuh"
 
 namespace dlrm {
 
-constexpr int kTile = 4096;          // sorted positions per CTA
-constexpr int kSortThreads = 256;    // 8 warps
-constexpr int kItems = kTile / kSortThreads;  // 16 per thread
-constexpr int kChunk = kTile / 8;    // 512 positions per warp in count/reduce
-constexpr int kRadixBits = 8;
-constexpr int kRadix = 1 << kRadixBits;
-constexpr int kMaxPasses = 4;
-constexpr uint32_t kSentinel = 0xffffffffu;
-constexpr uint32_t kHasHead = 1u, kHeadEnds = 2u, kHasTail = 4u;
-
 struct BwdLayout {
     size_t keys[2], vals[2], bag_of, uniq_table, uniq_row, seg_off, hist, counts, tstart, tile_base,
-        tile_count, tile_ubase, chunk_count, chunk_flags, chunk_tail_u, head, tail, num_unique, total;
+        tile_count, tile_ubase, chunk_flags, chunk_tail_u, head, tail, num_unique, total;
     int64_t ntiles_max, nchunks_max;
 };
 
@@ -53,7 +36,7 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
 {
     BwdLayout L{};
     L.ntiles_max = (nnz + kTile - 1) / kTile + T;
-    L.nchunks_max = L.ntiles_max * 8;
+    L.nchunks_max = L.ntiles_max * reduce_chunks_per_tile(d);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t at = off;
@@ -75,7 +58,6 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.tile_base = take(((size_t)T + 1) * 4);
     L.tile_count = take((size_t)L.ntiles_max * 4);
     L.tile_ubase = take((size_t)L.ntiles_max * 4);
-    L.chunk_count = take((size_t)L.nchunks_max * 4);
     L.chunk_flags = take((size_t)L.nchunks_max * 4);
     L.chunk_tail_u = take((size_t)L.nchunks_max * 4);
     L.head = take((size_t)L.nchunks_max * d * 4);
@@ -83,44 +65,6 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.num_unique = take(8);
     L.total = off;
     return L;
-}
-
-struct BwdPtrs {
-    uint32_t *keys[2], *vals[2], *bag_of, *uniq_row, *seg_off, *hist, *counts, *tstart, *tile_base,
-        *tile_count, *tile_ubase, *chunk_count, *chunk_flags, *chunk_tail_u;
-    int32_t *uniq_table;
-    float *head, *tail;
-    int64_t *num_unique;
-    int64_t ntiles_max;
-};
-
-struct TileInfo {
-    int t;
-    uint32_t lo, hi;
-    int valid;
-};
-
-// Table and position range of sort tile tau (thread 0; broadcast via smem).
-__device__ __forceinline__ void find_tile(int64_t tau, int T, const uint32_t *tile_base,
-                                          const uint32_t *tstart, TileInfo &ti)
-{
-    if (tau >= tile_base[T]) {
-        ti.valid = 0;
-        return;
-    }
-    int lo = 0, hi = T;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (tile_base[mid] <= tau)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    ti.t = lo;
-    ti.lo = tstart[lo] + (uint32_t)(tau - tile_base[lo]) * kTile;
-    const uint32_t end = tstart[lo + 1];
-    ti.hi = ti.lo + kTile < end ? ti.lo + kTile : end;
-    ti.valid = 1;
 }
 
 // ---------------------------------------------------------------- prep ---
@@ -390,6 +334,8 @@ sort_downsweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict_
 
 // ------------------------------------------------------ segment count ---
 
+// Number of run starts in each tile (the reduce numbers the runs of a tile
+// from the exclusive scan of these counts).
 __global__ void __launch_bounds__(256)
 seg_count_kernel(int T, int final_buf, BwdPtrs w)
 {
@@ -403,18 +349,14 @@ seg_count_kernel(int T, int final_buf, BwdPtrs w)
         return;
     const uint32_t *skey = w.keys[final_buf];
     const uint32_t ts = w.tstart[ti.t];
-    const uint32_t c0 = ti.lo + warp * kChunk;
-    const uint32_t c1 = c0 + kChunk < ti.hi ? c0 + kChunk : ti.hi;
     uint32_t count = 0;
-    for (uint32_t jb = c0; jb < c1; jb += 32) {
-        const uint32_t j = jb + lane;
-        const bool start = j < c1 && (j == ts || skey[j] != skey[j - 1]);
+    for (uint32_t jb = ti.lo; jb < ti.hi; jb += 256) {
+        const uint32_t j = jb + tid;
+        const bool start = j < ti.hi && run_starts(skey, j, ts);
         count += __popc(__ballot_sync(0xffffffffu, start));
     }
-    if (lane == 0) {
-        w.chunk_count[(size_t)blockIdx.x * 8 + warp] = count;
+    if (lane == 0)
         wc[warp] = count;
-    }
     __syncthreads();
     if (tid == 0) {
         uint32_t s = 0;
@@ -485,287 +427,6 @@ seg_scan_kernel(int T, int64_t nnz, BwdPtrs w)
     }
 }
 
-// ------------------------------------------------ reduce + row update ---
-
-struct ReduceArgs {
-    TableSet tables;  // written in place when lr != 0
-    int T, d;
-    int64_t B;
-    const float *dpooled;
-    int64_t dpss, dpts;
-    float lr;
-    float *grad_rows;
-    int64_t grad_cap;
-    int final_buf;
-    int32_t *err;
-};
-
-template <int VEC>
-struct Vec;
-template <>
-struct Vec<4> {
-    using F = float4;
-    __device__ __forceinline__ static F zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
-    __device__ __forceinline__ static F load(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
-    __device__ __forceinline__ static void store(float *p, const F &v) { *reinterpret_cast<float4 *>(p) = v; }
-    __device__ __forceinline__ static void add(F &a, const F &b) { a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w; }
-    __device__ __forceinline__ static float get(const F &v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
-};
-template <>
-struct Vec<1> {
-    using F = float;
-    __device__ __forceinline__ static F zero() { return 0.f; }
-    __device__ __forceinline__ static F load(const float *p) { return __ldg(p); }
-    __device__ __forceinline__ static void store(float *p, const F &v) { *p = v; }
-    __device__ __forceinline__ static void add(F &a, const F &b) { a += b; }
-    __device__ __forceinline__ static float get(const F &v, int) { return v; }
-};
-
-// SGD on VEC consecutive elements of one row: w <- w - lr * g, computed in
-// fp32 with one fused multiply-add and one rounding to the table type.
-template <typename TT, int VEC>
-__device__ __forceinline__ void sgd_update(TT *wrow, const typename Vec<VEC>::F &g, float lr)
-{
-    if constexpr (VEC == 4 && sizeof(TT) == 4) {
-        float4 wv = *reinterpret_cast<float4 *>(wrow);
-        wv.x = fmaf(-lr, g.x, wv.x);
-        wv.y = fmaf(-lr, g.y, wv.y);
-        wv.z = fmaf(-lr, g.z, wv.z);
-        wv.w = fmaf(-lr, g.w, wv.w);
-        *reinterpret_cast<float4 *>(wrow) = wv;
-    } else if constexpr (VEC == 4) {
-        uint2 raw = *reinterpret_cast<uint2 *>(wrow);
-        TT *h = reinterpret_cast<TT *>(&raw);
-#pragma unroll
-        for (int i = 0; i < 4; i++)
-            h[i] = from_f32<TT>(fmaf(-lr, Vec<4>::get(g, i), to_f32<TT>(h[i])));
-        *reinterpret_cast<uint2 *>(wrow) = raw;
-    } else {
-        wrow[0] = from_f32<TT>(fmaf(-lr, g, to_f32<TT>(wrow[0])));
-    }
-}
-
-template <typename TT, int VEC, int NV>
-__device__ __forceinline__ void apply_row(const ReduceArgs &a, int t, uint32_t u, uint32_t row,
-                                          int eb, int lane, const typename Vec<VEC>::F (&acc)[NV])
-{
-    if (a.grad_rows) {
-        if ((int64_t)u < a.grad_cap) {
-#pragma unroll
-            for (int v = 0; v < NV; v++) {
-                const int e = eb + (lane + 32 * v) * VEC;
-                if (e < a.d)
-                    Vec<VEC>::store(a.grad_rows + (int64_t)u * a.d + e, acc[v]);
-            }
-        } else if (lane == 0 && eb == 0) {
-            raise_flag(a.err, DLRM_FLAG_CAPACITY);
-        }
-    }
-    if (a.lr != 0.f && (int64_t)row < a.tables.rows[t]) {
-        TT *wrow = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t])) + (int64_t)row * a.d;
-#pragma unroll
-        for (int v = 0; v < NV; v++) {
-            const int e = eb + (lane + 32 * v) * VEC;
-            if (e < a.d)
-                sgd_update<TT, VEC>(wrow + e, acc[v], a.lr);
-        }
-    }
-}
-
-template <typename TT, int VEC, int NV>
-__global__ void __launch_bounds__(256)
-seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
-{
-    using V = Vec<VEC>;
-    using F = typename V::F;
-    constexpr int EB = 32 * VEC * NV;  // elements per pass over the chunk
-    constexpr int U = 8;               // gradient rows in flight per lane
-    __shared__ TileInfo ti;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0)
-        find_tile(blockIdx.x, a.T, w.tile_base, w.tstart, ti);
-    __syncthreads();
-    if (!ti.valid)
-        return;
-    const int t = ti.t;
-    const size_t ch = (size_t)blockIdx.x * 8 + warp;
-    const uint32_t c0 = ti.lo + warp * kChunk;
-    const uint32_t c1 = c0 + kChunk < ti.hi ? c0 + kChunk : ti.hi;
-    if (c0 >= c1) {
-        if (lane == 0)
-            w.chunk_flags[ch] = 0;
-        return;
-    }
-    const uint32_t *skey = w.keys[a.final_buf];
-    const uint32_t *sval = w.vals[a.final_buf];
-    const uint32_t ts = w.tstart[t], te = w.tstart[t + 1];
-    uint32_t ub = lane < warp ? w.chunk_count[(size_t)blockIdx.x * 8 + lane] : 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        ub += __shfl_xor_sync(0xffffffffu, ub, o);
-    ub += w.tile_ubase[blockIdx.x];
-    const bool carry_in = c0 > ts && skey[c0] == skey[c0 - 1];
-    const bool carry_out = c1 < te && skey[c1] == skey[c1 - 1];
-    const float *dpt = a.dpooled + (int64_t)t * a.dpts;
-    uint32_t flags = 0;
-
-    for (int eb = 0; eb < a.d; eb += EB) {
-        F acc[NV];
-#pragma unroll
-        for (int v = 0; v < NV; v++)
-            acc[v] = V::zero();
-        bool cur_carry = carry_in;
-        uint32_t cur_row = skey[c0], cur_u = 0, cur_start = c0, nseg = 0;
-
-        auto flush = [&](bool last) {
-            if (cur_carry) {
-#pragma unroll
-                for (int v = 0; v < NV; v++) {
-                    const int e = eb + (lane + 32 * v) * VEC;
-                    if (e < a.d)
-                        V::store(w.head + ch * a.d + e, acc[v]);
-                }
-                flags |= kHasHead | ((last && carry_out) ? 0u : kHeadEnds);
-            } else {
-                if (eb == 0 && lane == 0) {
-                    w.uniq_table[cur_u] = t;
-                    w.uniq_row[cur_u] = cur_row;
-                    w.seg_off[cur_u] = cur_start;
-                }
-                if (last && carry_out) {
-#pragma unroll
-                    for (int v = 0; v < NV; v++) {
-                        const int e = eb + (lane + 32 * v) * VEC;
-                        if (e < a.d)
-                            V::store(w.tail + ch * a.d + e, acc[v]);
-                    }
-                    flags |= kHasTail;
-                    if (eb == 0 && lane == 0)
-                        w.chunk_tail_u[ch] = cur_u;
-                } else {
-                    apply_row<TT, VEC, NV>(a, t, cur_u, cur_row, eb, lane, acc);
-                }
-            }
-#pragma unroll
-            for (int v = 0; v < NV; v++)
-                acc[v] = V::zero();
-        };
-
-        for (uint32_t jb = c0; jb < c1; jb += 32) {
-            const uint32_t j = jb + lane;
-            const bool valid = j < c1;
-            const uint32_t key_l = valid ? skey[j] : 0u;
-            const uint32_t pos_l = valid ? sval[j] : 0u;
-            const bool start_l = valid && (j == ts || key_l != skey[j - 1]);
-            uint32_t b_l = valid ? w.bag_of[pos_l] : 0u;
-            if (valid && (int64_t)b_l >= a.B) {
-                raise_flag(a.err, DLRM_FLAG_BAD_OFFSETS);
-                b_l = 0xffffffffu;
-            }
-            const unsigned startmask = __ballot_sync(0xffffffffu, start_l);
-            const int n = (int)(c1 - jb < 32 ? c1 - jb : 32);
-            for (int q = 0; q < n; q += U) {
-                F g[U][NV];
-#pragma unroll
-                for (int u = 0; u < U; u++) {
-                    const uint32_t bq = __shfl_sync(0xffffffffu, b_l, (q + u) & 31);
-                    const bool ok = (q + u) < n && bq != 0xffffffffu;
-                    const float *src = dpt + (int64_t)bq * a.dpss;
-#pragma unroll
-                    for (int v = 0; v < NV; v++) {
-                        const int e = eb + (lane + 32 * v) * VEC;
-                        g[u][v] = (ok && e < a.d) ? V::load(src + e) : V::zero();
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < U; u++) {
-                    const int src = q + u;
-                    if (src < n) {
-                        if ((startmask >> src) & 1u) {
-                            if (jb + src > c0)
-                                flush(false);
-                            cur_carry = false;
-                            cur_row = __shfl_sync(0xffffffffu, key_l, src);
-                            cur_start = jb + src;
-                            cur_u = ub + nseg;
-                            nseg++;
-                        }
-#pragma unroll
-                        for (int v = 0; v < NV; v++)
-                            V::add(acc[v], g[u][v]);
-                    }
-                }
-            }
-        }
-        flush(true);
-    }
-    if (lane == 0)
-        w.chunk_flags[ch] = flags;
-}
-
-// Runs that cross chunk boundaries: the owner (the chunk where the run
-// starts) adds the partial sums of the following chunks in order.
-template <typename TT, int VEC, int NV>
-__global__ void __launch_bounds__(256)
-seg_finalize_kernel(ReduceArgs a, BwdPtrs w)
-{
-    using V = Vec<VEC>;
-    using F = typename V::F;
-    constexpr int EB = 32 * VEC * NV;
-    const int lane = threadIdx.x & 31;
-    const size_t ch = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const size_t nch = (size_t)w.tile_base[a.T] * 8;
-    if (ch >= nch || !(w.chunk_flags[ch] & kHasTail))
-        return;
-    const uint32_t u = w.chunk_tail_u[ch];
-    const uint32_t row = w.uniq_row[u];
-    const int t = w.uniq_table[u];
-    for (int eb = 0; eb < a.d; eb += EB) {
-        F acc[NV];
-#pragma unroll
-        for (int v = 0; v < NV; v++) {
-            const int e = eb + (lane + 32 * v) * VEC;
-            acc[v] = e < a.d ? V::load(w.tail + ch * a.d + e) : V::zero();
-        }
-        bool done = false;
-        for (size_t c = ch + 1; !done && c < nch; c += 32) {
-            const size_t cc = c + lane;
-            const uint32_t f = cc < nch ? w.chunk_flags[cc] : (kHasHead | kHeadEnds);
-            const unsigned ends = __ballot_sync(0xffffffffu, (f & kHeadEnds) != 0);
-            const unsigned bad = __ballot_sync(0xffffffffu, (f & kHasHead) == 0);
-            int count = ends ? __ffs(ends) : 32;
-            if (bad) {
-                const int first_bad = __ffs(bad) - 1;
-                if (first_bad < count) {
-                    if (lane == 0)
-                        raise_flag(a.err, DLRM_FLAG_BAD_OFFSETS);
-                    count = first_bad;
-                    done = true;
-                }
-            }
-            for (int i0 = 0; i0 < count; i0 += 8) {
-                F g[8][NV];
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-#pragma unroll
-                    for (int v = 0; v < NV; v++) {
-                        const int e = eb + (lane + 32 * v) * VEC;
-                        g[i][v] = (i0 + i < count && e < a.d) ? V::load(w.head + (c + i0 + i) * a.d + e)
-                                                               : V::zero();
-                    }
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-#pragma unroll
-                    for (int v = 0; v < NV; v++)
-                        V::add(acc[v], g[i][v]);
-            }
-            if (ends)
-                done = true;
-        }
-        apply_row<TT, VEC, NV>(a, t, u, row, eb, lane, acc);
-    }
-}
-
 // ---------------------------------------------------------------- host ---
 
 static int row_bits(const TableSet &ts, int T)
@@ -777,28 +438,6 @@ static int row_bits(const TableSet &ts, int T)
     while (bits < 32 && ((int64_t)1 << bits) < maxr)
         bits++;
     return bits;
-}
-
-template <typename TT, int VEC, int NV>
-static int launch_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaStream_t st)
-{
-    seg_reduce_kernel<TT, VEC, NV><<<(unsigned)grid, 256, 0, st>>>(a, w);
-    count_launch(st);
-    int s = launch_status();
-    if (s != DLRM_OK)
-        return s;
-    seg_finalize_kernel<TT, VEC, NV><<<(unsigned)grid, 256, 0, st>>>(a, w);
-    count_launch(st);
-    return launch_status();
-}
-
-template <typename TT>
-static int launch_reduce_typed(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec,
-                               cudaStream_t st)
-{
-    if (vec)
-        return a.d <= 128 ? launch_reduce<TT, 4, 1>(a, w, grid, st) : launch_reduce<TT, 4, 2>(a, w, grid, st);
-    return launch_reduce<TT, 1, 4>(a, w, grid, st);
 }
 
 bool emb_bag_bwd_vectorisable(const TableSet &ts, int T, int d, const float *dpooled, int64_t dpss,
@@ -840,7 +479,6 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
     w.tile_base = reinterpret_cast<uint32_t *>(base + L.tile_base);
     w.tile_count = reinterpret_cast<uint32_t *>(base + L.tile_count);
     w.tile_ubase = reinterpret_cast<uint32_t *>(base + L.tile_ubase);
-    w.chunk_count = reinterpret_cast<uint32_t *>(base + L.chunk_count);
     w.chunk_flags = reinterpret_cast<uint32_t *>(base + L.chunk_flags);
     w.chunk_tail_u = reinterpret_cast<uint32_t *>(base + L.chunk_tail_u);
     w.head = reinterpret_cast<float *>(base + L.head);
@@ -919,14 +557,7 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
     a.grad_cap = grad_cap;
     a.final_buf = final_buf;
     a.err = err;
-    switch (dtype) {
-    case DLRM_F32:
-        return launch_reduce_typed<float>(a, w, grid, vec, st);
-    case DLRM_F16:
-        return launch_reduce_typed<__half>(a, w, grid, vec, st);
-    default:
-        return launch_reduce_typed<__nv_bfloat16>(a, w, grid, vec, st);
-    }
+    return launch_seg_reduce(dtype, a, w, grid, vec, st);
 }
 
 }  // namespace dlrm

@@ -1,0 +1,84 @@
+// Shared definitions of the embedding-bag backward (coalescing sort, segmented
+// reduce, row-wise SGD).
+#pragma once
+
+#include "common.cuh"
+
+namespace dlrm {
+
+constexpr int kTile = 4096;                   // sorted positions per tile
+constexpr int kSortThreads = 256;             // 8 warps
+constexpr int kItems = kTile / kSortThreads;  // 16 per thread
+constexpr int kRadixBits = 8;
+constexpr int kRadix = 1 << kRadixBits;
+constexpr int kMaxPasses = 4;
+constexpr uint32_t kSentinel = 0xffffffffu;   // sort key of an out-of-range index
+constexpr uint32_t kHasHead = 1u, kHeadEnds = 2u, kHasTail = 4u;
+constexpr int kReduceThreads = 256;           // 8 warps per tile in the reduce, one chunk each
+
+// Reduce chunks per tile (the layout of the partial sums is sized for it).
+inline int reduce_chunks_per_tile(int) { return kReduceThreads / 32; }
+
+struct BwdPtrs {
+    uint32_t *keys[2], *vals[2], *bag_of, *uniq_row, *seg_off, *hist, *counts, *tstart, *tile_base,
+        *tile_count, *tile_ubase, *chunk_flags, *chunk_tail_u;
+    int32_t *uniq_table;
+    float *head, *tail;
+    int64_t *num_unique;
+    int64_t ntiles_max;
+};
+
+struct TileInfo {
+    int t;
+    uint32_t lo, hi;
+    int valid;
+};
+
+// Table and position range of tile tau (tiles never straddle a table).
+__device__ __forceinline__ void find_tile(int64_t tau, int T, const uint32_t *tile_base,
+                                          const uint32_t *tstart, TileInfo &ti)
+{
+    if (tau >= tile_base[T]) {
+        ti.valid = 0;
+        return;
+    }
+    int lo = 0, hi = T;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tile_base[mid] <= tau)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    ti.t = lo;
+    ti.lo = tstart[lo] + (uint32_t)(tau - tile_base[lo]) * kTile;
+    const uint32_t end = tstart[lo + 1];
+    ti.hi = ti.lo + kTile < end ? ti.lo + kTile : end;
+    ti.valid = 1;
+}
+
+// A sorted position starts a run when it is the first lookup of its table
+// or its row differs from the previous sorted row.
+__device__ __forceinline__ bool run_starts(const uint32_t *skey, uint32_t j, uint32_t table_start)
+{
+    return j == table_start || skey[j] != skey[j - 1];
+}
+
+struct ReduceArgs {
+    TableSet tables;  // written in place when lr != 0
+    int T, d;
+    int64_t B;
+    const float *dpooled;
+    int64_t dpss, dpts;
+    float lr;
+    float *grad_rows;
+    int64_t grad_cap;
+    int final_buf;
+    int32_t *err;
+};
+
+// Segmented reduce + SGD and the combine of cross-chunk runs (seg_reduce.cu).
+int launch_seg_reduce(int dtype, const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec,
+                      cudaStream_t st);
+
+}  // namespace dlrm

@@ -7,23 +7,28 @@
 // Design: a group of G lanes (G = 4..32) owns one bag at a time; each lane
 // owns one or more 16-byte chunks of the row, so a row is read as one fully
 // coalesced burst of 16-byte loads.  The group loads up to G indices of its
-// bag at once (one per lane, streaming), then walks them with shuffles,
-// keeping U rows in flight per lane before accumulating in fp32.  Bags are
-// visited in table-major order, so at any moment the warps of the GPU touch
-// the same few tables and hot (Zipf) rows stay in L2.  The pooled vector is
-// written once with streaming stores.  Grid: persistent, resident blocks only.
+// bag at once (one per lane, streaming) and each lane checks its own index
+// against the table, so the walk over the bag only broadcasts 32-bit rows
+// (one shuffle per lookup) and keeps 8 rows in flight per lane; the fp32 sums
+// use packed adds.  The kernel stays within 64 registers, so 32 warps share
+// an SM and hide the gather latency.  Bags are visited in table-major order,
+// so at any moment the warps of the GPU touch the same few tables and hot
+// (Zipf) rows stay in L2.  The pooled vector is written once with streaming
+// stores.  Grid: persistent, resident blocks only.
 #include "common.cuh"
 
 namespace dlrm {
 
-template <typename TT, int G, int MAXCH, int U>
-__global__ void __launch_bounds__(256)
+template <typename TT, int G, int C, int U>
+__global__ void __launch_bounds__(256, 4)
 emb_bag_fwd_vec_kernel(TableSet ts, int T, int nchunks, const int64_t *__restrict__ offsets,
                        const int64_t *__restrict__ indices, int64_t nnz, int64_t B,
                        float *__restrict__ out, int64_t oss, int64_t ots, int32_t *err)
 {
     constexpr int EPC = Chunk16<TT>::kElems;  // elements per 16-byte chunk
     constexpr int GPW = 32 / G;               // bags per warp
+    constexpr uint32_t kBad = 0xffffffffu;    // row slot without a valid lookup
+    static_assert(U <= G && G % U == 0, "a group walks its G indices in steps of U");
     const int lane = threadIdx.x & 31;
     const int gl = lane % G;
     const int grp = lane / G;
@@ -31,6 +36,11 @@ emb_bag_fwd_vec_kernel(TableSet ts, int T, int nchunks, const int64_t *__restric
     const int64_t nbags = (int64_t)T * B;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    bool chunk_on[C];
+#pragma unroll
+    for (int c = 0; c < C; c++)
+        chunk_on[c] = c * G + gl < nchunks;
+    const uint32_t row_bytes = (uint32_t)nchunks * 16;
 
     for (int64_t bag = warp * GPW + grp; bag < nbags; bag += nwarps * GPW) {
         const int t = (int)(bag / B);
@@ -42,57 +52,54 @@ emb_bag_fwd_vec_kernel(TableSet ts, int T, int nchunks, const int64_t *__restric
                 raise_flag(err, DLRM_FLAG_BAD_OFFSETS);
             k0 = k1 = 0;
         }
-        const char *tab = static_cast<const char *>(ts.ptr[t]);
+        const char *tab = static_cast<const char *>(ts.ptr[t]) + gl * 16;  // this lane's first piece
         const int64_t R = ts.rows[t];
-        const int64_t row_bytes = (int64_t)nchunks * 16;
 
-        float acc[MAXCH][EPC];
+        float2 acc[C][EPC / 2];
 #pragma unroll
-        for (int c = 0; c < MAXCH; c++)
+        for (int c = 0; c < C; c++)
 #pragma unroll
-            for (int e = 0; e < EPC; e++)
-                acc[c][e] = 0.f;
+            for (int e = 0; e < EPC / 2; e++)
+                acc[c][e] = make_float2(0.f, 0.f);
 
         for (int64_t kb = k0; kb < k1; kb += G) {
             const int n = (k1 - kb < G) ? (int)(k1 - kb) : G;
-            const int64_t my_idx = (gl < n) ? load_stream(indices + kb + gl) : 0;
+            // each lane checks one index; invalid ones and the slots past the
+            // bag's end read nothing
+            uint32_t row = kBad;
+            if (gl < n) {
+                const int64_t r = load_stream(indices + kb + gl);
+                if (r >= 0 && r < R)
+                    row = (uint32_t)r;
+                else
+                    raise_flag(err, DLRM_FLAG_INDEX_OOB);
+            }
             for (int q = 0; q < n; q += U) {
-                uint4 v[U][MAXCH];
+                uint4 v[U][C];
 #pragma unroll
                 for (int u = 0; u < U; u++) {
-                    const int64_t r = __shfl_sync(gmask, my_idx, (q + u) & (G - 1), G);
-                    bool ok = (q + u) < n;
-                    if (ok && (r < 0 || r >= R)) {
-                        if (gl == 0)
-                            raise_flag(err, DLRM_FLAG_INDEX_OOB);
-                        ok = false;
-                    }
+                    const uint32_t r = __shfl_sync(gmask, row, q + u, G);
+                    const char *p = tab + (size_t)r * row_bytes;
 #pragma unroll
-                    for (int c = 0; c < MAXCH; c++) {
-                        const int chunk = gl + c * G;
-                        if (ok && chunk < nchunks)
-                            v[u][c] = load_table(tab + r * row_bytes + (int64_t)chunk * 16);
-                        else
-                            v[u][c] = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                    for (int c = 0; c < C; c++)
+                        v[u][c] = (r != kBad && chunk_on[c]) ? load_table(p + c * G * 16) : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
                 for (int u = 0; u < U; u++)
 #pragma unroll
-                    for (int c = 0; c < MAXCH; c++)
+                    for (int c = 0; c < C; c++)
                         Chunk16<TT>::add(acc[c], v[u][c]);
             }
         }
 
         float *o = out + b * oss + (int64_t)t * ots;
 #pragma unroll
-        for (int c = 0; c < MAXCH; c++) {
-            const int chunk = gl + c * G;
-            if (chunk < nchunks) {
-                float4 *dst = reinterpret_cast<float4 *>(o + (int64_t)chunk * EPC);
+        for (int c = 0; c < C; c++) {
+            if (chunk_on[c]) {
+                float4 *dst = reinterpret_cast<float4 *>(o + (int64_t)(c * G + gl) * EPC);
 #pragma unroll
-                for (int e = 0; e < EPC; e += 4)
-                    __stcs(dst + e / 4, make_float4(acc[c][e], acc[c][e + 1], acc[c][e + 2], acc[c][e + 3]));
+                for (int e = 0; e < EPC / 4; e++)
+                    __stcs(dst + e, make_float4(acc[c][2 * e].x, acc[c][2 * e].y, acc[c][2 * e + 1].x, acc[c][2 * e + 1].y));
             }
         }
     }
@@ -150,13 +157,16 @@ static int grid_for(K kernel, int64_t work_blocks)
     return (int)(work_blocks < resident ? (work_blocks < 1 ? 1 : work_blocks) : resident);
 }
 
-template <typename TT, int G, int MAXCH>
+template <typename TT, int G, int C>
 static int launch_vec(const TableSet &ts, int T, int nchunks, const int64_t *offsets,
                       const int64_t *indices, int64_t nnz, int64_t B, float *out, int64_t oss,
                       int64_t ots, int32_t *err, cudaStream_t st)
 {
-    constexpr int U = MAXCH == 1 ? 8 : (MAXCH == 2 ? 4 : 2);
-    auto kernel = emb_bag_fwd_vec_kernel<TT, G, MAXCH, U>;
+    // 8 x 16 bytes in flight per lane; half-precision rows need twice the
+    // accumulators, so wide half rows keep fewer in flight
+    constexpr int U0 = (C == 1 ? 8 : (C == 2 ? 4 : 2)) / ((Chunk16<TT>::kElems == 8 && C > 1) ? 2 : 1);
+    constexpr int U = U0 < G ? U0 : G;
+    auto kernel = emb_bag_fwd_vec_kernel<TT, G, C, U>;
     const int64_t bags_per_block = 8 * (32 / G);
     const int grid = grid_for(kernel, ((int64_t)T * B + bags_per_block - 1) / bags_per_block);
     kernel<<<grid, 256, 0, st>>>(ts, T, nchunks, offsets, indices, nnz, B, out, oss, ots, err);

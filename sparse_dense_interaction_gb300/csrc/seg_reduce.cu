@@ -1,0 +1,364 @@
+// Segmented reduce of pooled-vector gradients over runs of equal rows, and
+// the row-wise SGD update of each unique row (the embedding-bag backward of
+// "Notes/DLRM", vault-aram.pages.dev: section 2's per-feature lookups are
+// summed, so every lookup of a row receives its bag's pooled gradient;
+// section 5: the rows are then trained, here by plain SGD).
+//
+// Design.  One CTA per sort tile (4096 sorted lookups of one table):
+//  A. the CTA stages the tile's sorted rows and, through the position of each
+//     lookup, its bag id in shared memory, marks where runs of equal rows
+//     start, counts the starts of every chunk and numbers the runs;
+//  B. each warp walks one chunk of 512 sorted lookups; a lane owns one 16-byte
+//     piece of each pooled-gradient row (32 lanes x 16 B = 128 fp32 values
+//     per pass), 4 rows in flight, fp32 sums with packed adds.  The kernel
+//     is kept lean (at most 64 registers, so 4 CTAs of 8 warps share an SM and
+//     hide the latency of the row gathers); when a run ends its table row
+//     is read, updated (w - lr*g, one rounding to the table type) and
+//     written, once per unique row.  Runs that cross a chunk boundary leave
+//     partial sums that the finalize kernel adds in chunk order, so results
+//     are deterministic.
+#include <type_traits>
+
+#include "emb_bag_bwd.cuh"
+
+namespace dlrm {
+
+// VEC fp32 gradient values of one lane, added with packed fp32 adds.
+template <int VEC>
+struct Vec;
+template <>
+struct Vec<4> {
+    using F = float4;
+    __device__ __forceinline__ static F zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ __forceinline__ static F load(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+    __device__ __forceinline__ static void store(float *p, const F &v) { *reinterpret_cast<float4 *>(p) = v; }
+    __device__ __forceinline__ static void add(F &a, const F &b)
+    {
+        const float2 lo = __fadd2_rn(make_float2(a.x, a.y), make_float2(b.x, b.y));
+        const float2 hi = __fadd2_rn(make_float2(a.z, a.w), make_float2(b.z, b.w));
+        a = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    __device__ __forceinline__ static float get(const F &v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+};
+template <>
+struct Vec<1> {
+    using F = float;
+    __device__ __forceinline__ static F zero() { return 0.f; }
+    __device__ __forceinline__ static F load(const float *p) { return __ldg(p); }
+    __device__ __forceinline__ static void store(float *p, const F &v) { *p = v; }
+    __device__ __forceinline__ static void add(F &a, const F &b) { a += b; }
+    __device__ __forceinline__ static float get(const F &v, int) { return v; }
+};
+
+// VEC consecutive table elements of one lane.
+template <typename TT, int VEC>
+struct RowChunk {
+    static constexpr int kBytes = (int)sizeof(TT) * VEC;
+    using R = typename std::conditional<
+        kBytes == 16, uint4,
+        typename std::conditional<kBytes == 8, uint2,
+                                  typename std::conditional<kBytes == 4, uint32_t, uint16_t>::type>::type>::type;
+    __device__ __forceinline__ static R load(const TT *p) { return *reinterpret_cast<const R *>(p); }
+    __device__ __forceinline__ static void store(TT *p, const R &r) { *reinterpret_cast<R *>(p) = r; }
+    // w <- w - lr * g in fp32 (one fused multiply-add), rounded once to TT
+    __device__ __forceinline__ static R sgd(R r, const typename Vec<VEC>::F &g, float lr)
+    {
+        TT *h = reinterpret_cast<TT *>(&r);
+#pragma unroll
+        for (int i = 0; i < VEC; i++)
+            h[i] = from_f32<TT>(fmaf(-lr, Vec<VEC>::get(g, i), to_f32<TT>(h[i])));
+        return r;
+    }
+};
+
+template <typename TT, int VEC, int U>
+__global__ void __launch_bounds__(kReduceThreads, 4)
+seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
+{
+    using V = Vec<VEC>;
+    using F = typename V::F;
+    using RC = RowChunk<TT, VEC>;
+    constexpr int NS = kReduceThreads / 32;      // chunks per tile, one warp each
+    constexpr int CW = kTile / NS;               // sorted lookups per chunk
+    constexpr int EB = 32 * VEC;                 // row elements per pass
+    constexpr int PER = kTile / kReduceThreads;  // staged lookups per thread
+    constexpr uint32_t kStart = 0x80000000u;     // bag word: a run starts here
+    constexpr uint32_t kNoBag = 0x7fffffffu;     // bag word: no valid bag
+
+    __shared__ uint2 skb[kTile];  // sorted row, bag of the lookup | kStart at run starts
+    __shared__ uint32_t cbase[NS];
+    __shared__ TileInfo ti;
+    __shared__ uint32_t key_before, key_after;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0)
+        find_tile(blockIdx.x, a.T, w.tile_base, w.tstart, ti);
+    if (tid < NS)
+        cbase[tid] = 0;
+    __syncthreads();
+    if (!ti.valid)
+        return;
+    const int t = ti.t;
+    const uint32_t lo = ti.lo, n = ti.hi - ti.lo;
+    const uint32_t ts = w.tstart[t], te = w.tstart[t + 1];
+    const uint32_t *skey = w.keys[a.final_buf];
+    const uint32_t *sval = w.vals[a.final_buf];
+    if (tid == 0) {
+        key_before = lo > ts ? skey[lo - 1] : 0u;
+        key_after = ti.hi < te ? skey[ti.hi] : 0u;
+    }
+
+    // A. stage rows and bag ids (8 lookups per thread in flight)
+    for (int r0 = 0; r0 < PER; r0 += 8) {
+        uint32_t pos[8];
+#pragma unroll
+        for (int r = 0; r < 8; r++) {
+            const uint32_t i = (uint32_t)(r0 + r) * kReduceThreads + tid;
+            pos[r] = 0;
+            if (i < n) {
+                skb[i].x = skey[lo + i];
+                pos[r] = sval[lo + i];
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 8; r++) {
+            const uint32_t i = (uint32_t)(r0 + r) * kReduceThreads + tid;
+            if (i < n) {
+                uint32_t b = w.bag_of[pos[r]];
+                if ((int64_t)b >= a.B) {
+                    raise_flag(a.err, DLRM_FLAG_BAD_OFFSETS);
+                    b = kNoBag;
+                }
+                skb[i].y = b;
+            }
+        }
+    }
+    __syncthreads();
+    // run starts, counted per chunk (each warp step covers 32 consecutive lookups)
+    for (int r = 0; r < PER; r++) {
+        const uint32_t i = (uint32_t)r * kReduceThreads + tid;
+        bool st = false;
+        if (i < n) {
+            st = lo + i == ts || skb[i].x != (i == 0 ? key_before : skb[i - 1].x);
+            if (st)
+                skb[i].y |= kStart;
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, st);
+        if (lane == 0 && bal)
+            atomicAdd(&cbase[((uint32_t)r * kReduceThreads + warp * 32) / CW], (uint32_t)__popc(bal));
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t v = lane < NS ? cbase[lane] : 0u;
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += x;
+        }
+        if (lane < NS)
+            cbase[lane] = w.tile_ubase[blockIdx.x] + incl - v;
+    }
+    __syncthreads();
+
+    // B. one warp per chunk, one 16-byte piece of each gradient row per lane
+    const size_t ch = (size_t)blockIdx.x * NS + warp;
+    const uint32_t c0 = (uint32_t)warp * CW;
+    const uint32_t c1 = c0 + CW < n ? c0 + CW : n;
+    if (c0 >= c1) {
+        if (lane == 0)
+            w.chunk_flags[ch] = 0;
+        return;
+    }
+    const bool carry_in = !(skb[c0].y & kStart);
+    const bool carry_out = c1 < n ? !(skb[c1].y & kStart) : (ti.hi < te && key_after == skb[n - 1].x);
+    const uint32_t ub = cbase[warp];
+    const bool update = a.lr != 0.f;
+    TT *wtab = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t]));
+    const int64_t rows_t = a.tables.rows[t];
+    uint32_t flags = 0;
+
+    for (int eb = 0; eb < a.d; eb += EB) {
+        const int e = eb + lane * VEC;
+        const bool lane_on = e < a.d;
+        const float *dpt = a.dpooled + (int64_t)t * a.dpts + e;
+        F acc = V::zero();
+        bool cur_carry = carry_in;
+        uint32_t cur_row = 0, cur_u = 0, cur_start = lo + c0, nseg = 0;
+
+        auto flush = [&](bool last) {
+            if (cur_carry) {
+                if (lane_on)
+                    V::store(w.head + ch * a.d + e, acc);
+                flags |= kHasHead | ((last && carry_out) ? 0u : kHeadEnds);
+            } else {
+                if (eb == 0 && lane == 0) {
+                    w.uniq_table[cur_u] = t;
+                    w.uniq_row[cur_u] = cur_row;
+                    w.seg_off[cur_u] = cur_start;
+                }
+                if (last && carry_out) {
+                    if (lane_on)
+                        V::store(w.tail + ch * a.d + e, acc);
+                    flags |= kHasTail;
+                    if (eb == 0 && lane == 0)
+                        w.chunk_tail_u[ch] = cur_u;
+                } else {
+                    if (a.grad_rows) {
+                        if ((int64_t)cur_u < a.grad_cap) {
+                            if (lane_on)
+                                V::store(a.grad_rows + (int64_t)cur_u * a.d + e, acc);
+                        } else if (lane == 0 && eb == 0) {
+                            raise_flag(a.err, DLRM_FLAG_CAPACITY);
+                        }
+                    }
+                    if (update && lane_on && (int64_t)cur_row < rows_t) {
+                        TT *wp = wtab + (int64_t)cur_row * a.d + e;
+                        RC::store(wp, RC::sgd(RC::load(wp), acc, a.lr));
+                    }
+                }
+            }
+            acc = V::zero();
+        };
+
+        for (uint32_t p0 = c0; p0 < c1; p0 += U) {
+            uint2 kb[U];
+            F g[U];
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                kb[u] = p0 + u < c1 ? skb[p0 + u] : make_uint2(0u, kNoBag);
+                const uint32_t b = kb[u].y & ~kStart;
+                g[u] = (b != kNoBag && lane_on) ? V::load(dpt + (int64_t)b * a.dpss) : V::zero();
+            }
+            if (update && lane_on) {
+                // table rows of the runs that start in the next step, into L1
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    const uint32_t q = p0 + U + u;
+                    if (q < c1) {
+                        const uint2 nk = skb[q];
+                        if ((nk.y & kStart) && (int64_t)nk.x < rows_t)
+                            asm volatile("prefetch.global.L1 [%0];" ::"l"(wtab + (int64_t)nk.x * a.d + e));
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                if (kb[u].y & kStart) {
+                    if (p0 + u > c0)
+                        flush(false);
+                    cur_carry = false;
+                    cur_row = kb[u].x;
+                    cur_start = lo + p0 + u;
+                    cur_u = ub + nseg;
+                    nseg++;
+                }
+                V::add(acc, g[u]);
+            }
+        }
+        flush(true);
+    }
+    if (lane == 0)
+        w.chunk_flags[ch] = flags;
+}
+
+// Runs that cross chunk boundaries: one warp per owner chunk (the chunk where
+// the run starts) adds the partial sums of the following chunks in chunk
+// order, 32 chunk flags at a time, then applies the update.
+template <typename TT, int VEC>
+__global__ void __launch_bounds__(256)
+seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
+{
+    using V = Vec<VEC>;
+    using F = typename V::F;
+    constexpr int EB = 32 * VEC;
+    const int lane = threadIdx.x & 31;
+    const size_t nch = (size_t)w.tile_base[a.T] * NS;
+    const size_t nwarps = (size_t)gridDim.x * (blockDim.x / 32);
+    for (size_t ch = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); ch < nch; ch += nwarps) {
+        if (!(w.chunk_flags[ch] & kHasTail))
+            continue;
+        const uint32_t u = w.chunk_tail_u[ch];
+        const uint32_t row = w.uniq_row[u];
+        const int t = w.uniq_table[u];
+        for (int eb = 0; eb < a.d; eb += EB) {
+            const int e = eb + lane * VEC;
+            F acc = e < a.d ? V::load(w.tail + ch * a.d + e) : V::zero();
+            bool done = false;
+            for (size_t c = ch + 1; !done && c < nch; c += 32) {
+                const size_t cc = c + lane;
+                const uint32_t f = cc < nch ? w.chunk_flags[cc] : (kHasHead | kHeadEnds);
+                const unsigned ends = __ballot_sync(0xffffffffu, (f & kHeadEnds) != 0);
+                const unsigned bad = __ballot_sync(0xffffffffu, (f & kHasHead) == 0);
+                int count = ends ? __ffs(ends) : 32;
+                if (bad) {
+                    const int first_bad = __ffs(bad) - 1;
+                    if (first_bad < count) {
+                        if (lane == 0)
+                            raise_flag(a.err, DLRM_FLAG_BAD_OFFSETS);
+                        count = first_bad;
+                        done = true;
+                    }
+                }
+                for (int i0 = 0; i0 < count; i0 += 8) {
+                    F g[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++)
+                        g[i] = (i0 + i < count && e < a.d) ? V::load(w.head + (c + i0 + i) * a.d + e) : V::zero();
+#pragma unroll
+                    for (int i = 0; i < 8; i++)
+                        V::add(acc, g[i]);
+                }
+                if (ends)
+                    done = true;
+            }
+            if (e < a.d) {
+                if (a.grad_rows) {
+                    if ((int64_t)u < a.grad_cap)
+                        V::store(a.grad_rows + (int64_t)u * a.d + e, acc);
+                    else if (lane == 0 && eb == 0)
+                        raise_flag(a.err, DLRM_FLAG_CAPACITY);
+                }
+                if (a.lr != 0.f && (int64_t)row < a.tables.rows[t]) {
+                    TT *wp = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t])) + (int64_t)row * a.d + e;
+                    RowChunk<TT, VEC>::store(wp, RowChunk<TT, VEC>::sgd(RowChunk<TT, VEC>::load(wp), acc, a.lr));
+                }
+            }
+        }
+    }
+}
+
+template <typename TT, int VEC, int U>
+static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaStream_t st)
+{
+    seg_reduce_kernel<TT, VEC, U><<<(unsigned)grid, kReduceThreads, 0, st>>>(a, w);
+    count_launch(st);
+    int s = launch_status();
+    if (s != DLRM_OK)
+        return s;
+    constexpr int NS = kReduceThreads / 32;
+    const int64_t warps = grid * NS;  // one warp per chunk
+    seg_finalize_kernel<TT, VEC><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, w, NS);
+    count_launch(st);
+    return launch_status();
+}
+
+template <typename TT>
+static int reduce_typed(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
+{
+    return vec ? run_reduce<TT, 4, 4>(a, w, grid, st) : run_reduce<TT, 1, 8>(a, w, grid, st);
+}
+
+int launch_seg_reduce(int dtype, const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
+{
+    switch (dtype) {
+    case DLRM_F32:
+        return reduce_typed<float>(a, w, grid, vec, st);
+    case DLRM_F16:
+        return reduce_typed<__half>(a, w, grid, vec, st);
+    default:
+        return reduce_typed<__nv_bfloat16>(a, w, grid, vec, st);
+    }
+}
+
+}  // namespace dlrm
