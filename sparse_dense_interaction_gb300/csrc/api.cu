@@ -191,6 +191,8 @@ int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d,
         return DLRM_ERR_UNSUPPORTED;
     if (B == 0 && nnz != 0)  // no bags cannot hold lookups
         return DLRM_ERR_INVALID_ARG;
+    if (dp_sample_stride > ((int64_t)1 << 29))  // the reduce addresses pooled rows with 32-bit byte strides
+        return DLRM_ERR_UNSUPPORTED;
     if (!(lr == lr))  // NaN learning rate
         return DLRM_ERR_INVALID_ARG;
     if (!offsets || !workspace || !aligned(workspace, 256) || !aligned(offsets, 8))

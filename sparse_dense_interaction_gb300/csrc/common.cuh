@@ -31,8 +31,8 @@ __device__ __forceinline__ void raise_flag(int32_t *flag, int bits)
         atomicOr(flag, bits);
 }
 
-// 16-byte table chunk added into fp32 accumulators (kElems/2 float2 pairs),
-// with packed fp32 adds.
+// 16-byte table chunk added into fp32 accumulators (kElems/2 float2 pairs).
+// fp32 chunks use packed fp32 adds.
 template <typename TT>
 struct Chunk16;
 
@@ -46,6 +46,8 @@ struct Chunk16<float> {
     }
 };
 
+// Half-precision chunks use mixed-precision adds (the 16-bit operand is
+// widened exactly inside the add), one instruction per element.
 template <>
 struct Chunk16<__half> {
     static constexpr int kElems = 8;
@@ -54,7 +56,8 @@ struct Chunk16<__half> {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; i++)
-            acc[i] = __fadd2_rn(acc[i], __half22float2(*reinterpret_cast<const __half2 *>(&w[i])));
+            asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.f16 %0, lo, %0; add.rn.f32.f16 %1, hi, %1; }"
+                : "+f"(acc[i].x), "+f"(acc[i].y) : "r"(w[i]));
     }
 };
 
@@ -65,8 +68,9 @@ struct Chunk16<__nv_bfloat16> {
     {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; i++)  // bf16 -> fp32 is exact: the bf16 bits are the top half of the word
-            acc[i] = __fadd2_rn(acc[i], make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)));
+        for (int i = 0; i < 4; i++)
+            asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; add.rn.f32.bf16 %0, lo, %0; add.rn.f32.bf16 %1, hi, %1; }"
+                : "+f"(acc[i].x), "+f"(acc[i].y) : "r"(w[i]));
     }
 };
 

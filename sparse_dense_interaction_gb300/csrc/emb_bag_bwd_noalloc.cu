@@ -86,6 +86,8 @@ extern "C" int dlrm_emb_bag_bwd_sgd_noalloc(void *const *tables, const int64_t *
         return DLRM_ERR_UNSUPPORTED;
     if (B == 0 && nnz != 0)
         return DLRM_ERR_INVALID_ARG;
+    if (dp_sample_stride > ((int64_t)1 << 29))  // the reduce addresses pooled rows with 32-bit byte strides
+        return DLRM_ERR_UNSUPPORTED;
     if (!(lr == lr))
         return DLRM_ERR_INVALID_ARG;
     if (!offsets || reinterpret_cast<uintptr_t>(offsets) % 8 != 0)

@@ -10,7 +10,7 @@
 //     start, counts the starts of every chunk and numbers the runs;
 //  B. each warp walks one chunk of 512 sorted lookups; a lane owns one 16-byte
 //     piece of each pooled-gradient row (32 lanes x 16 B = 128 fp32 values
-//     per pass), 4 rows in flight, fp32 sums with packed adds.  The kernel
+//     per pass), 8 rows in flight, fp32 sums with packed adds.  The kernel
 //     is kept lean (at most 64 registers, so 4 CTAs of 8 warps share an SM and
 //     hide the latency of the row gathers); when a run ends its table row
 //     is read, updated (w - lr*g, one rounding to the table type) and
@@ -106,6 +106,9 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
         key_before = lo > ts ? skey[lo - 1] : 0u;
         key_after = ti.hi < te ? skey[ti.hi] : 0u;
     }
+    const bool update = a.lr != 0.f;
+    TT *wtab = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t]));
+    const int64_t rows_t = a.tables.rows[t];
 
     // A. stage rows and bag ids (8 lookups per thread in flight)
     for (int r0 = 0; r0 < PER; r0 += 8) {
@@ -146,6 +149,10 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
         if (lane == 0 && bal)
             atomicAdd(&cbase[((uint32_t)r * kReduceThreads + warp * 32) / CW], (uint32_t)__popc(bal));
     }
+    // pad the tile to a whole number of steps with lookups that contribute
+    // nothing and start no run, so the walk below needs no bounds checks
+    if (tid < (int)((U - n % U) % U))  // n is then below kTile, a multiple of U
+        skb[n + tid] = make_uint2(0u, kNoBag);
     __syncthreads();
     if (warp == 0) {
         const uint32_t v = lane < NS ? cbase[lane] : 0u;
@@ -173,15 +180,13 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     const bool carry_in = !(skb[c0].y & kStart);
     const bool carry_out = c1 < n ? !(skb[c1].y & kStart) : (ti.hi < te && key_after == skb[n - 1].x);
     const uint32_t ub = cbase[warp];
-    const bool update = a.lr != 0.f;
-    TT *wtab = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t]));
-    const int64_t rows_t = a.tables.rows[t];
     uint32_t flags = 0;
 
     for (int eb = 0; eb < a.d; eb += EB) {
         const int e = eb + lane * VEC;
         const bool lane_on = e < a.d;
-        const float *dpt = a.dpooled + (int64_t)t * a.dpts + e;
+        const char *dpt_bytes = reinterpret_cast<const char *>(a.dpooled + (int64_t)t * a.dpts + e);
+        const uint32_t dpss_bytes = (uint32_t)a.dpss * 4u;
         F acc = V::zero();
         bool cur_carry = carry_in;
         uint32_t cur_row = 0, cur_u = 0, cur_start = lo + c0, nseg = 0;
@@ -220,35 +225,26 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
             }
             acc = V::zero();
         };
-
-        for (uint32_t p0 = c0; p0 < c1; p0 += U) {
-            uint2 kb[U];
+        const uint32_t c1e = c1 + (U - c1 % U) % U;  // padded end of the walk
+        for (uint32_t p0 = c0; p0 < c1e; p0 += U) {
             F g[U];
+            uint32_t starts = 0;  // bit u: a run starts at p0 + u
 #pragma unroll
             for (int u = 0; u < U; u++) {
-                kb[u] = p0 + u < c1 ? skb[p0 + u] : make_uint2(0u, kNoBag);
-                const uint32_t b = kb[u].y & ~kStart;
-                g[u] = (b != kNoBag && lane_on) ? V::load(dpt + (int64_t)b * a.dpss) : V::zero();
-            }
-            if (update && lane_on) {
-                // table rows of the runs that start in the next step, into L1
-#pragma unroll
-                for (int u = 0; u < U; u++) {
-                    const uint32_t q = p0 + U + u;
-                    if (q < c1) {
-                        const uint2 nk = skb[q];
-                        if ((nk.y & kStart) && (int64_t)nk.x < rows_t)
-                            asm volatile("prefetch.global.L1 [%0];" ::"l"(wtab + (int64_t)nk.x * a.d + e));
-                    }
-                }
+                const uint32_t by = skb[p0 + u].y;
+                starts |= (by >> 31) << u;
+                const uint32_t b = by & ~kStart;
+                g[u] = V::zero();
+                if (b != kNoBag && lane_on)
+                    g[u] = V::load(reinterpret_cast<const float *>(dpt_bytes + (uint64_t)b * dpss_bytes));
             }
 #pragma unroll
             for (int u = 0; u < U; u++) {
-                if (kb[u].y & kStart) {
+                if ((starts >> u) & 1u) {
                     if (p0 + u > c0)
                         flush(false);
                     cur_carry = false;
-                    cur_row = kb[u].x;
+                    cur_row = skb[p0 + u].x;
                     cur_start = lo + p0 + u;
                     cur_u = ub + nseg;
                     nseg++;
@@ -346,7 +342,7 @@ static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaS
 template <typename TT>
 static int reduce_typed(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
 {
-    return vec ? run_reduce<TT, 4, 4>(a, w, grid, st) : run_reduce<TT, 1, 8>(a, w, grid, st);
+    return vec ? run_reduce<TT, 4, 8>(a, w, grid, st) : run_reduce<TT, 1, 8>(a, w, grid, st);
 }
 
 int launch_seg_reduce(int dtype, const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
