@@ -10,7 +10,7 @@
 //     start, counts the starts of every chunk and numbers the runs;
 //  B. each warp walks one chunk of 512 sorted lookups; a lane owns one 16-byte
 //     piece of each pooled-gradient row (32 lanes x 16 B = 128 fp32 values
-//     per pass), 8 rows in flight, fp32 sums with packed adds.  The kernel
+//     per pass), 4 rows in flight, fp32 sums with packed adds.  The kernel
 //     is kept lean (at most 64 registers, so 4 CTAs of 8 warps share an SM and
 //     hide the latency of the row gathers); when a run ends its table row
 //     is read, updated (w - lr*g, one rounding to the table type) and
@@ -342,7 +342,7 @@ static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaS
 template <typename TT>
 static int reduce_typed(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
 {
-    return vec ? run_reduce<TT, 4, 8>(a, w, grid, st) : run_reduce<TT, 1, 8>(a, w, grid, st);
+    return vec ? run_reduce<TT, 4, 4>(a, w, grid, st) : run_reduce<TT, 1, 8>(a, w, grid, st);
 }
 
 int launch_seg_reduce(int dtype, const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
