@@ -6,8 +6,10 @@
 //
 // Forward design: a CTA takes S samples.  The F x d block Z of each sample
 // (row 0 = e0, rows 1..N = pooled embeddings) is staged through shared memory
-// in chunks of KC = 32 columns, transposed to [k][i] so that four consecutive
-// rows of one column are one 16-byte load.  Each thread owns one 4 x 4 tile of
+// in chunks of KC = 32 columns: each row chunk is one coalesced 128-byte read
+// (4 lanes x 32 bytes), transposed to [k][i] (column groups XOR-swizzled by k
+// so the transposing stores are conflict-free) so that four consecutive rows
+// of one column are one 16-byte load.  Each thread owns one 4 x 4 tile of
 // the lower triangle of Z Z^T and accumulates it in registers over all
 // chunks (16 FMAs per two 16-byte shared loads; lanes of a warp share tile
 // rows and columns, so those loads are broadcasts).  The triangle is staged
@@ -47,6 +49,15 @@ __device__ __forceinline__ void load8(const float *src, int k, int d, bool vec, 
     }
 }
 
+// Position of element (k, i) in a staged row of TS columns (TS a multiple
+// of 32): 4-column groups are XOR-swizzled by bits 3..4 of k, so the
+// transposing stores of 8 rows x 4 column octets from one warp hit 32
+// distinct banks, while 4 consecutive columns stay one aligned 16-byte word.
+__device__ __forceinline__ int zt_col(int k, int i)
+{
+    return ((((i >> 2) ^ (((k >> 3) & 3) << 1))) << 2) | (i & 3);
+}
+
 __global__ void __launch_bounds__(1024)
 interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__restrict__ emb,
                     int64_t embs, int N, int d, int64_t B, int inc, float *__restrict__ y,
@@ -55,11 +66,12 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
     extern __shared__ __align__(16) float smem[];
     const int F = N + 1;
     const int Fp = (F + 3) & ~3;
+    const int TS = (Fp + 31) & ~31;                     // staged row: Fp columns, swizzled
     const int nTR = Fp / 4;
     const int ntiles = nTR * (nTR + 1) / 2;
     const int64_t P = inc ? (int64_t)F * (F + 1) / 2 : (int64_t)F * (F - 1) / 2;
-    float *Zt = smem;                                   // [S][kKC][Fp]
-    float *ybuf = Zt + (size_t)S * kKC * Fp;            // [S][P]
+    float *Zt = smem;                                   // [S][kKC][TS], transposed chunk of Z
+    float *ybuf = Zt + (size_t)S * kKC * TS;            // [S][P]
     uint8_t *tileI = reinterpret_cast<uint8_t *>(ybuf + (size_t)S * P);
     uint8_t *tileJ = tileI + ntiles;
     const int tid = threadIdx.x;
@@ -84,13 +96,17 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
             acc[r][c] = 0.f;
 
     const bool vec_y = vec_out != 0;
-    const int groups = kKC / 8;
+    const int rblocks = (F + 7) / 8;
     for (int kc = 0; kc < d; kc += kKC) {
-        for (int li = tid; li < S * groups * F; li += blockDim.x) {
-            const int i = li % F;
-            const int rem = li / F;
-            const int q = rem % groups;
-            const int ss = rem / groups;
+        // stage: a warp reads 8 rows x 4 column octets (32 bytes per lane, so
+        // each row chunk is one coalesced 128-byte read) and transposes them
+        for (int li = tid; li < S * rblocks * 32; li += blockDim.x) {
+            const int lane = li & 31;
+            const int i = ((li >> 5) % rblocks) * 8 + (lane & 7);
+            const int q = lane >> 3;
+            const int ss = (li >> 5) / rblocks;
+            if (i >= F)
+                continue;
             const int64_t b = b0 + ss;
             const int k = kc + 8 * q;
             float v[8];
@@ -113,20 +129,20 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
                 for (int m = 0; m < 8; m++)
                     v[m] = 0.f;
             }
-            float *zt = Zt + (size_t)ss * kKC * Fp + (size_t)(8 * q) * Fp + i;
+            float *zt = Zt + (size_t)ss * kKC * TS;
 #pragma unroll
             for (int m = 0; m < 8; m++)
-                zt[(size_t)m * Fp] = v[m];
+                zt[(8 * q + m) * TS + zt_col(8 * q + m, i)] = v[m];
         }
         __syncthreads();
         if (active) {
             const int I = tileI[tile], J = tileJ[tile];
-            const float *zs = Zt + (size_t)s * kKC * Fp;
+            const float *zs = Zt + (size_t)s * kKC * TS;
             const int kn = min(kKC, d - kc);
 #pragma unroll 4
             for (int k = 0; k < kn; k++) {
-                const float4 a = *reinterpret_cast<const float4 *>(zs + (size_t)k * Fp + 4 * I);
-                const float4 bb = *reinterpret_cast<const float4 *>(zs + (size_t)k * Fp + 4 * J);
+                const float4 a = *reinterpret_cast<const float4 *>(zs + (size_t)k * TS + zt_col(k, 4 * I));
+                const float4 bb = *reinterpret_cast<const float4 *>(zs + (size_t)k * TS + zt_col(k, 4 * J));
                 const float av[4] = {a.x, a.y, a.z, a.w};
                 const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
@@ -294,7 +310,8 @@ int launch_interact_fwd(const float *e0, int64_t e0s, const float *emb, int64_t 
     const int nTR = Fp / 4;
     const int ntiles = nTR * (nTR + 1) / 2;
     const int64_t P = num_pairs_of(F, inc);
-    const size_t per_sample = ((size_t)kKC * Fp + (size_t)P) * sizeof(float);
+    const int TS = (Fp + 31) & ~31;
+    const size_t per_sample = ((size_t)kKC * TS + (size_t)P) * sizeof(float);
     int S = ntiles >= 256 ? 1 : 256 / ntiles;
     while (S > 1 && (size_t)S * per_sample > 96 * 1024)
         S--;
