@@ -7,7 +7,8 @@
 //
 // Pipeline (all on the caller's stream, no host synchronisation):
 //  1. prep       table start positions from the CSR offsets, tiles per table
-//  2. bag ids    bag number of every lookup position (4 bytes per lookup)
+//  2. bag ids    bag number of every lookup position (4 bytes per lookup,
+//                written coalesced)
 //  3. sort       stable LSD radix sort of (row, position) pairs, segmented by
 //                table: the CSR input is already grouped by table, so tiles
 //                never straddle a table and only the row bits are sorted
@@ -109,21 +110,46 @@ bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t n
 
 // ------------------------------------------------------------- bag ids ---
 
+// A warp takes 32 consecutive bags; each lane finds the bag of a lookup
+// position by binary search over the 33 offsets held in the warp's lanes, so
+// the bag ids are written as coalesced 128-byte rows.
 __global__ void __launch_bounds__(256)
 bag_ids_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nnz,
                uint32_t *__restrict__ bag_of, int32_t *err)
 {
+    const int lane = threadIdx.x & 31;
     const int64_t nbags = (int64_t)T * B;
-    for (int64_t bag = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; bag < nbags;
-         bag += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t k0 = offsets[bag], k1 = offsets[bag + 1];
-        if (k0 < 0 || k1 < k0 || k1 > nnz) {
-            raise_flag(err, DLRM_FLAG_BAD_OFFSETS);
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t g0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32; g0 < nbags; g0 += nwarps * 32) {
+        const int64_t bag = g0 + lane;
+        // start of this lane's bag; lanes past the last bag never match
+        int64_t o = bag <= nbags ? offsets[bag] : nnz + 1;
+        const int64_t last = g0 + 32 < nbags ? g0 + 32 : nbags;
+        const int64_t end = offsets[last];
+        const int64_t next = __shfl_down_sync(0xffffffffu, o, 1);
+        const bool bad = bag < last && (o < 0 || o > nnz || (lane < 31 ? next : end) < o);
+        if (__any_sync(0xffffffffu, bad)) {
+            if (lane == 0)
+                raise_flag(err, DLRM_FLAG_BAD_OFFSETS);
             continue;
         }
-        const uint32_t b = (uint32_t)(bag % B);
-        for (int64_t k = k0; k < k1; k++)
-            bag_of[k] = b;
+        if (bag > last)
+            o = nnz + 1;
+        const int64_t start = __shfl_sync(0xffffffffu, o, 0);
+        // warp-uniform trip count: every lane takes part in every shuffle
+        for (int64_t p0 = start; p0 < end; p0 += 32) {
+            const int64_t p = p0 + lane;
+            int l = 0;
+#pragma unroll
+            for (int step = 16; step > 0; step >>= 1) {
+                const int cand = l + step;
+                const int64_t oc = __shfl_sync(0xffffffffu, o, cand & 31);
+                if (cand < 32 && oc <= p)
+                    l = cand;
+            }
+            if (p < end)
+                bag_of[p] = (uint32_t)((g0 + l) % B);
+        }
     }
 }
 
@@ -509,7 +535,7 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
     }
     {
         const int64_t nbags = (int64_t)T * B;
-        int64_t grid = (nbags + 255) / 256;
+        int64_t grid = (nbags + 255) / 256;  // 8 warps of 32 bags per block
         const int64_t cap = (int64_t)sm_count() * 8;
         bag_ids_kernel<<<(unsigned)(grid < cap ? grid : cap), 256, 0, st>>>(offsets, T, B, nnz, w.bag_of, err);
         count_launch(st);
