@@ -359,7 +359,7 @@ def bwd_kernel_names(passes):
     names = list(BWD_KERNELS_PREFIX)
     for p in range(passes):
         names += [f"sort_upsweep[{p}]", f"sort_scan[{p}]", f"sort_downsweep[{p}]"]
-    return names + ["seg_count", "seg_scan", "seg_reduce", "seg_finalize"]
+    return names + ["seg_count", "seg_scan", "seg_reduce", "seg_block_sum", "seg_finalize"]
 
 
 def algorithmic_bytes(cfg, st):

@@ -27,7 +27,7 @@ namespace dlrm {
 
 struct BwdLayout {
     size_t keys[2], vals[2], bag_of, uniq_table, uniq_row, seg_off, hist, counts, tstart, tile_base,
-        tile_count, tile_ubase, chunk_flags, chunk_tail_u, head, tail, num_unique, total;
+        tile_count, tile_ubase, chunk_flags, chunk_tail_u, head, tail, block_flags, block_sum, num_unique, total;
     int64_t ntiles_max, nchunks_max;
 };
 
@@ -63,6 +63,9 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.chunk_tail_u = take((size_t)L.nchunks_max * 4);
     L.head = take((size_t)L.nchunks_max * d * 4);
     L.tail = take((size_t)L.nchunks_max * d * 4);
+    const int64_t nblocks = L.nchunks_max / kFinalizeBlock + 1;
+    L.block_flags = take((size_t)nblocks * 4);
+    L.block_sum = take((size_t)nblocks * d * 4);
     L.num_unique = take(8);
     L.total = off;
     return L;
@@ -509,6 +512,8 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
     w.chunk_tail_u = reinterpret_cast<uint32_t *>(base + L.chunk_tail_u);
     w.head = reinterpret_cast<float *>(base + L.head);
     w.tail = reinterpret_cast<float *>(base + L.tail);
+    w.block_flags = reinterpret_cast<uint32_t *>(base + L.block_flags);
+    w.block_sum = reinterpret_cast<float *>(base + L.block_sum);
     w.num_unique = reinterpret_cast<int64_t *>(base + L.num_unique);
     w.ntiles_max = L.ntiles_max;
 

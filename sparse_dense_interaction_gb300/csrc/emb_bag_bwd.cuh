@@ -15,15 +15,16 @@ constexpr int kMaxPasses = 4;
 constexpr uint32_t kSentinel = 0xffffffffu;   // sort key of an out-of-range index
 constexpr uint32_t kHasHead = 1u, kHeadEnds = 2u, kHasTail = 4u;
 constexpr int kReduceThreads = 256;           // 8 warps per tile in the reduce, one chunk each
+constexpr int kFinalizeBlock = 32;            // chunks summed per block in the finalize's first level
 
 // Reduce chunks per tile (the layout of the partial sums is sized for it).
 inline int reduce_chunks_per_tile(int) { return kReduceThreads / 32; }
 
 struct BwdPtrs {
     uint32_t *keys[2], *vals[2], *bag_of, *uniq_row, *seg_off, *hist, *counts, *tstart, *tile_base,
-        *tile_count, *tile_ubase, *chunk_flags, *chunk_tail_u;
+        *tile_count, *tile_ubase, *chunk_flags, *chunk_tail_u, *block_flags;
     int32_t *uniq_table;
-    float *head, *tail;
+    float *head, *tail, *block_sum;
     int64_t *num_unique;
     int64_t ntiles_max;
 };

@@ -15,8 +15,8 @@
 //     hide the latency of the row gathers); when a run ends its table row
 //     is read, updated (w - lr*g, one rounding to the table type) and
 //     written, once per unique row.  Runs that cross a chunk boundary leave
-//     partial sums that the finalize kernel adds in chunk order, so results
-//     are deterministic.
+//     partial sums, which two small kernels combine in chunk order (block
+//     sums of 32 chunks, then the run's owner), so results are deterministic.
 #include <type_traits>
 
 #include "emb_bag_bwd.cuh"
@@ -258,9 +258,84 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
         w.chunk_flags[ch] = flags;
 }
 
-// Runs that cross chunk boundaries: one warp per owner chunk (the chunk where
-// the run starts) adds the partial sums of the following chunks in chunk
-// order, 32 chunk flags at a time, then applies the update.
+// Runs that cross chunk boundaries are combined in two levels, all sums in
+// chunk order (deterministic).  Level 1: one warp per block of 32 chunks sums
+// the partials of the run that enters the block at its first chunk, up to that
+// run's end or the block's end.  Level 2: the warp of the chunk where a run
+// starts adds the partials of the following chunks up to the next block
+// boundary, then one block sum per block, and applies the update.
+constexpr uint32_t kBlockEnters = 1u, kBlockEnds = 2u;
+
+// Sums chunk partials head[c0 .. c0 + count) into acc, 8 loads in flight.
+template <int VEC>
+__device__ __forceinline__ void add_heads(typename Vec<VEC>::F &acc, const float *head, size_t c0, int count,
+                                          int d, int e)
+{
+    using V = Vec<VEC>;
+    for (int i0 = 0; i0 < count; i0 += 8) {
+        typename V::F g[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            g[i] = (i0 + i < count && e < d) ? V::load(head + (c0 + i0 + i) * d + e) : V::zero();
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            V::add(acc, g[i]);
+    }
+}
+
+// Number of chunk flags from c (at most `limit`) to add for a run that
+// continues into chunk c: up to and including the first chunk where it ends.
+// Sets ends when the run ends within them; flags a chunk without a partial.
+__device__ __forceinline__ int run_extent(const uint32_t *flags, size_t c, int limit, bool &ends, int lane,
+                                          int32_t *err)
+{
+    const uint32_t f = lane < limit ? flags[c + lane] : kHasHead;
+    const unsigned endm = __ballot_sync(0xffffffffu, lane < limit && (f & kHeadEnds));
+    const unsigned bad = __ballot_sync(0xffffffffu, lane < limit && !(f & kHasHead));
+    int count = endm ? __ffs(endm) : limit;
+    ends = endm != 0;
+    if (bad && __ffs(bad) - 1 < count) {
+        if (lane == 0)
+            raise_flag(err, DLRM_FLAG_BAD_OFFSETS);
+        count = __ffs(bad) - 1;
+        ends = true;
+    }
+    return count;
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(256)
+seg_block_sum_kernel(ReduceArgs a, BwdPtrs w, int NS)
+{
+    using V = Vec<VEC>;
+    using F = typename V::F;
+    constexpr int EB = 32 * VEC;
+    const int lane = threadIdx.x & 31;
+    const size_t nch = (size_t)w.tile_base[a.T] * NS;
+    const size_t nblk = (nch + kFinalizeBlock - 1) / kFinalizeBlock;
+    const size_t nwarps = (size_t)gridDim.x * (blockDim.x / 32);
+    for (size_t blk = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); blk < nblk; blk += nwarps) {
+        const size_t c0 = blk * kFinalizeBlock;
+        if (!(w.chunk_flags[c0] & kHasHead)) {
+            if (lane == 0)
+                w.block_flags[blk] = 0;
+            continue;
+        }
+        const int limit = (int)(nch - c0 < (size_t)kFinalizeBlock ? nch - c0 : kFinalizeBlock);
+        bool ends;
+        const int count = run_extent(w.chunk_flags, c0, limit, ends, lane, a.err);
+        for (int eb = 0; eb < a.d; eb += EB) {
+            const int e = eb + lane * VEC;
+            F acc = V::zero();
+            add_heads<VEC>(acc, w.head, c0, count, a.d, e);
+            if (e < a.d)
+                V::store(w.block_sum + blk * a.d + e, acc);
+        }
+        if (lane == 0)
+            w.block_flags[blk] = kBlockEnters | (ends ? kBlockEnds : 0u);
+    }
+}
+
 template <typename TT, int VEC>
 __global__ void __launch_bounds__(256)
 seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
@@ -270,6 +345,7 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
     constexpr int EB = 32 * VEC;
     const int lane = threadIdx.x & 31;
     const size_t nch = (size_t)w.tile_base[a.T] * NS;
+    const size_t nblk = (nch + kFinalizeBlock - 1) / kFinalizeBlock;
     const size_t nwarps = (size_t)gridDim.x * (blockDim.x / 32);
     for (size_t ch = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); ch < nch; ch += nwarps) {
         if (!(w.chunk_flags[ch] & kHasTail))
@@ -277,37 +353,36 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
         const uint32_t u = w.chunk_tail_u[ch];
         const uint32_t row = w.uniq_row[u];
         const int t = w.uniq_table[u];
+        // chunks up to the next block boundary, one by one
+        const size_t c1 = ch + 1;
+        const size_t bound = ((c1 + kFinalizeBlock - 1) / kFinalizeBlock) * kFinalizeBlock;
+        const size_t stop = bound < nch ? bound : nch;
+        bool ends = c1 >= nch;
+        int count = 0;
+        if (!ends && stop > c1)
+            count = run_extent(w.chunk_flags, c1, (int)(stop - c1), ends, lane, a.err);
+        // then whole blocks: their flags 32 at a time
+        size_t first_blk = stop / kFinalizeBlock, nblocks_run = 0;
+        for (size_t blk = first_blk; !ends && blk < nblk; blk += 32) {
+            const uint32_t bf = blk + lane < nblk ? w.block_flags[blk + lane] : (kBlockEnters | kBlockEnds);
+            const unsigned endm = __ballot_sync(0xffffffffu, (bf & kBlockEnds) != 0);
+            const unsigned bad = __ballot_sync(0xffffffffu, (bf & kBlockEnters) == 0);
+            int n = endm ? __ffs(endm) : 32;
+            if (bad && __ffs(bad) - 1 < n) {
+                if (lane == 0)
+                    raise_flag(a.err, DLRM_FLAG_BAD_OFFSETS);
+                n = __ffs(bad) - 1;
+                ends = true;
+            }
+            nblocks_run += n;
+            if (endm)
+                ends = true;
+        }
         for (int eb = 0; eb < a.d; eb += EB) {
             const int e = eb + lane * VEC;
             F acc = e < a.d ? V::load(w.tail + ch * a.d + e) : V::zero();
-            bool done = false;
-            for (size_t c = ch + 1; !done && c < nch; c += 32) {
-                const size_t cc = c + lane;
-                const uint32_t f = cc < nch ? w.chunk_flags[cc] : (kHasHead | kHeadEnds);
-                const unsigned ends = __ballot_sync(0xffffffffu, (f & kHeadEnds) != 0);
-                const unsigned bad = __ballot_sync(0xffffffffu, (f & kHasHead) == 0);
-                int count = ends ? __ffs(ends) : 32;
-                if (bad) {
-                    const int first_bad = __ffs(bad) - 1;
-                    if (first_bad < count) {
-                        if (lane == 0)
-                            raise_flag(a.err, DLRM_FLAG_BAD_OFFSETS);
-                        count = first_bad;
-                        done = true;
-                    }
-                }
-                for (int i0 = 0; i0 < count; i0 += 8) {
-                    F g[8];
-#pragma unroll
-                    for (int i = 0; i < 8; i++)
-                        g[i] = (i0 + i < count && e < a.d) ? V::load(w.head + (c + i0 + i) * a.d + e) : V::zero();
-#pragma unroll
-                    for (int i = 0; i < 8; i++)
-                        V::add(acc, g[i]);
-                }
-                if (ends)
-                    done = true;
-            }
+            add_heads<VEC>(acc, w.head, c1, count, a.d, e);
+            add_heads<VEC>(acc, w.block_sum, first_blk, (int)nblocks_run, a.d, e);
             if (e < a.d) {
                 if (a.grad_rows) {
                     if ((int64_t)u < a.grad_cap)
@@ -334,6 +409,11 @@ static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaS
         return s;
     constexpr int NS = kReduceThreads / 32;
     const int64_t warps = grid * NS;  // one warp per chunk
+    const int64_t blocks = (warps + kFinalizeBlock - 1) / kFinalizeBlock;  // one warp per block of chunks
+    seg_block_sum_kernel<VEC><<<(unsigned)((blocks + 7) / 8), 256, 0, st>>>(a, w, NS);
+    count_launch(st);
+    if ((s = launch_status()) != DLRM_OK)
+        return s;
     seg_finalize_kernel<TT, VEC><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, w, NS);
     count_launch(st);
     return launch_status();
