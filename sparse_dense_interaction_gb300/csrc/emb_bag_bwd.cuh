@@ -17,8 +17,9 @@ constexpr uint32_t kHasHead = 1u, kHeadEnds = 2u, kHasTail = 4u;
 constexpr int kReduceThreads = 256;           // 8 warps per tile in the reduce, one chunk each
 constexpr int kFinalizeBlock = 32;            // chunks summed per block in the finalize's first level
 
-// Reduce chunks per tile (the layout of the partial sums is sized for it).
-inline int reduce_chunks_per_tile(int) { return kReduceThreads / 32; }
+// Reduce chunks per tile (the layout of the partial sums is sized for it):
+// one per stream of 16 or 32 lanes.
+inline int reduce_chunks_per_tile(int) { return (kReduceThreads / 32) * 2; }
 
 struct BwdPtrs {
     uint32_t *keys[2], *vals[2], *bag_of, *uniq_row, *seg_off, *hist, *counts, *tstart, *tile_base,

@@ -71,19 +71,33 @@ struct RowChunk {
     }
 };
 
-template <typename TT, int VEC, int U>
+// Asks L2 to fetch the line holding p (no register result, never faults the
+// caller: only called on rows inside the table).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// G lanes form a stream that walks one chunk; each lane owns C pieces of VEC
+// fp32 values of every gradient row (piece c of lane l covers elements
+// (c*G + l)*VEC ..), U lookups in flight per stream.  With the update on, the
+// table rows of runs that start PD steps ahead are prefetched into L2, so the
+// read-modify-write at a run's end finds its row there.
+template <typename TT, int VEC, int G, int C, int U, int PD>
 __global__ void __launch_bounds__(kReduceThreads, 4)
 seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
 {
     using V = Vec<VEC>;
     using F = typename V::F;
     using RC = RowChunk<TT, VEC>;
-    constexpr int NS = kReduceThreads / 32;      // chunks per tile, one warp each
-    constexpr int CW = kTile / NS;               // sorted lookups per chunk
-    constexpr int EB = 32 * VEC;                 // row elements per pass
-    constexpr int PER = kTile / kReduceThreads;  // staged lookups per thread
-    constexpr uint32_t kStart = 0x80000000u;     // bag word: a run starts here
-    constexpr uint32_t kNoBag = 0x7fffffffu;     // bag word: no valid bag
+    constexpr int S = 32 / G;                      // streams per warp
+    constexpr int NS = (kReduceThreads / 32) * S;  // chunks per tile, one stream each
+    constexpr int CW = kTile / NS;                 // sorted lookups per chunk
+    constexpr int EB = G * C * VEC;                // row elements per pass
+    constexpr int PER = kTile / kReduceThreads;    // staged lookups per thread
+    constexpr uint32_t kStart = 0x80000000u;       // bag word: a run starts here
+    constexpr uint32_t kNoBag = 0x7fffffffu;       // bag word: no valid bag
+    static_assert(NS <= 32 && CW % 32 == 0, "chunk geometry");
 
     __shared__ uint2 skb[kTile];  // sorted row, bag of the lookup | kStart at run starts
     __shared__ uint32_t cbase[NS];
@@ -168,75 +182,115 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     }
     __syncthreads();
 
-    // B. one warp per chunk, one 16-byte piece of each gradient row per lane
-    const size_t ch = (size_t)blockIdx.x * NS + warp;
-    const uint32_t c0 = (uint32_t)warp * CW;
+    // B. one stream of G lanes per chunk
+    const int sidx = warp * S + lane / G;
+    const int gl = lane % G;
+    const size_t ch = (size_t)blockIdx.x * NS + sidx;
+    const uint32_t c0 = (uint32_t)sidx * CW;
     const uint32_t c1 = c0 + CW < n ? c0 + CW : n;
     if (c0 >= c1) {
-        if (lane == 0)
+        if (gl == 0)
             w.chunk_flags[ch] = 0;
         return;
     }
     const bool carry_in = !(skb[c0].y & kStart);
     const bool carry_out = c1 < n ? !(skb[c1].y & kStart) : (ti.hi < te && key_after == skb[n - 1].x);
-    const uint32_t ub = cbase[warp];
+    const uint32_t ub = cbase[sidx];
     uint32_t flags = 0;
 
     for (int eb = 0; eb < a.d; eb += EB) {
-        const int e = eb + lane * VEC;
-        const bool lane_on = e < a.d;
-        const char *dpt_bytes = reinterpret_cast<const char *>(a.dpooled + (int64_t)t * a.dpts + e);
+        bool on[C];
+#pragma unroll
+        for (int c = 0; c < C; c++)
+            on[c] = eb + (c * G + gl) * VEC < a.d;
+        const char *dpt_bytes = reinterpret_cast<const char *>(a.dpooled + (int64_t)t * a.dpts + eb + gl * VEC);
         const uint32_t dpss_bytes = (uint32_t)a.dpss * 4u;
-        F acc = V::zero();
+        F acc[C];
+#pragma unroll
+        for (int c = 0; c < C; c++)
+            acc[c] = V::zero();
         bool cur_carry = carry_in;
         uint32_t cur_row = 0, cur_u = 0, cur_start = lo + c0, nseg = 0;
 
         auto flush = [&](bool last) {
             if (cur_carry) {
-                if (lane_on)
-                    V::store(w.head + ch * a.d + e, acc);
+#pragma unroll
+                for (int c = 0; c < C; c++)
+                    if (on[c])
+                        V::store(w.head + ch * a.d + eb + (c * G + gl) * VEC, acc[c]);
                 flags |= kHasHead | ((last && carry_out) ? 0u : kHeadEnds);
             } else {
-                if (eb == 0 && lane == 0) {
+                if (eb == 0 && gl == 0) {
                     w.uniq_table[cur_u] = t;
                     w.uniq_row[cur_u] = cur_row;
                     w.seg_off[cur_u] = cur_start;
                 }
                 if (last && carry_out) {
-                    if (lane_on)
-                        V::store(w.tail + ch * a.d + e, acc);
+#pragma unroll
+                    for (int c = 0; c < C; c++)
+                        if (on[c])
+                            V::store(w.tail + ch * a.d + eb + (c * G + gl) * VEC, acc[c]);
                     flags |= kHasTail;
-                    if (eb == 0 && lane == 0)
+                    if (eb == 0 && gl == 0)
                         w.chunk_tail_u[ch] = cur_u;
                 } else {
                     if (a.grad_rows) {
                         if ((int64_t)cur_u < a.grad_cap) {
-                            if (lane_on)
-                                V::store(a.grad_rows + (int64_t)cur_u * a.d + e, acc);
-                        } else if (lane == 0 && eb == 0) {
+#pragma unroll
+                            for (int c = 0; c < C; c++)
+                                if (on[c])
+                                    V::store(a.grad_rows + (int64_t)cur_u * a.d + eb + (c * G + gl) * VEC, acc[c]);
+                        } else if (gl == 0 && eb == 0) {
                             raise_flag(a.err, DLRM_FLAG_CAPACITY);
                         }
                     }
-                    if (update && lane_on && (int64_t)cur_row < rows_t) {
-                        TT *wp = wtab + (int64_t)cur_row * a.d + e;
-                        RC::store(wp, RC::sgd(RC::load(wp), acc, a.lr));
+                    if (update && (int64_t)cur_row < rows_t) {
+#pragma unroll
+                        for (int c = 0; c < C; c++)
+                            if (on[c]) {
+                                TT *wp = wtab + (int64_t)cur_row * a.d + eb + (c * G + gl) * VEC;
+                                RC::store(wp, RC::sgd(RC::load(wp), acc[c], a.lr));
+                            }
                     }
                 }
             }
-            acc = V::zero();
+#pragma unroll
+            for (int c = 0; c < C; c++)
+                acc[c] = V::zero();
         };
+
         const uint32_t c1e = c1 + (U - c1 % U) % U;  // padded end of the walk
         for (uint32_t p0 = c0; p0 < c1e; p0 += U) {
-            F g[U];
+            if (PD > 0 && update) {
+#pragma unroll
+                for (int u = 0; u < U; u++) {
+                    const uint32_t q = p0 + PD * U + u;
+                    if (q < c1) {
+                        const uint2 kb = skb[q];
+                        if ((kb.y & kStart) && (int64_t)kb.x < rows_t) {
+                            const TT *wr = wtab + (int64_t)kb.x * a.d + eb + gl * VEC;
+#pragma unroll
+                            for (int c = 0; c < C; c++)
+                                if (on[c])
+                                    prefetch_l2(wr + c * G * VEC);
+                        }
+                    }
+                }
+            }
+            F g[U][C];
             uint32_t starts = 0;  // bit u: a run starts at p0 + u
 #pragma unroll
             for (int u = 0; u < U; u++) {
                 const uint32_t by = skb[p0 + u].y;
                 starts |= (by >> 31) << u;
                 const uint32_t b = by & ~kStart;
-                g[u] = V::zero();
-                if (b != kNoBag && lane_on)
-                    g[u] = V::load(reinterpret_cast<const float *>(dpt_bytes + (uint64_t)b * dpss_bytes));
+                const float *src = reinterpret_cast<const float *>(dpt_bytes + (uint64_t)b * dpss_bytes);
+#pragma unroll
+                for (int c = 0; c < C; c++) {
+                    g[u][c] = V::zero();
+                    if (b != kNoBag && on[c])
+                        g[u][c] = V::load(src + c * G * VEC);
+                }
             }
 #pragma unroll
             for (int u = 0; u < U; u++) {
@@ -249,12 +303,14 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                     cur_u = ub + nseg;
                     nseg++;
                 }
-                V::add(acc, g[u]);
+#pragma unroll
+                for (int c = 0; c < C; c++)
+                    V::add(acc[c], g[u][c]);
             }
         }
         flush(true);
     }
-    if (lane == 0)
+    if (gl == 0)
         w.chunk_flags[ch] = flags;
 }
 
@@ -399,22 +455,22 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
     }
 }
 
-template <typename TT, int VEC, int U>
+template <typename TT, int VEC, int G, int C, int U, int PD>
 static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaStream_t st)
 {
-    seg_reduce_kernel<TT, VEC, U><<<(unsigned)grid, kReduceThreads, 0, st>>>(a, w);
+    seg_reduce_kernel<TT, VEC, G, C, U, PD><<<(unsigned)grid, kReduceThreads, 0, st>>>(a, w);
     count_launch(st);
     int s = launch_status();
     if (s != DLRM_OK)
         return s;
-    constexpr int NS = kReduceThreads / 32;
-    const int64_t warps = grid * NS;  // one warp per chunk
-    const int64_t blocks = (warps + kFinalizeBlock - 1) / kFinalizeBlock;  // one warp per block of chunks
+    constexpr int NS = (kReduceThreads / 32) * (32 / G);
+    const int64_t chunks = grid * NS;
+    const int64_t blocks = (chunks + kFinalizeBlock - 1) / kFinalizeBlock;  // one warp per block of chunks
     seg_block_sum_kernel<VEC><<<(unsigned)((blocks + 7) / 8), 256, 0, st>>>(a, w, NS);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
-    seg_finalize_kernel<TT, VEC><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a, w, NS);
+    seg_finalize_kernel<TT, VEC><<<(unsigned)((chunks + 7) / 8), 256, 0, st>>>(a, w, NS);
     count_launch(st);
     return launch_status();
 }
@@ -422,7 +478,10 @@ static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaS
 template <typename TT>
 static int reduce_typed(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
 {
-    return vec ? run_reduce<TT, 4, 4>(a, w, grid, st) : run_reduce<TT, 1, 8>(a, w, grid, st);
+    if (!vec)
+        return run_reduce<TT, 1, 32, 1, 8, 0>(a, w, grid, st);
+    // rows of 32+ pieces: half-warp streams with two pieces per lane
+    return a.d >= 128 ? run_reduce<TT, 4, 16, 2, 2, 1>(a, w, grid, st) : run_reduce<TT, 4, 32, 1, 4, 1>(a, w, grid, st);
 }
 
 int launch_seg_reduce(int dtype, const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
