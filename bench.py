@@ -356,9 +356,8 @@ BWD_KERNELS_PREFIX = ["bwd_prep", "bag_ids"]
 
 
 def bwd_kernel_names(passes):
-    names = list(BWD_KERNELS_PREFIX)
-    for p in range(passes):
-        names += [f"sort_upsweep[{p}]", f"sort_scan[{p}]", f"sort_downsweep[{p}]"]
+    names = list(BWD_KERNELS_PREFIX) + ["sort_hist", "sort_digit_scan"]
+    names += [f"sort_pass[{p}]" for p in range(passes)]
     return names + ["seg_count", "seg_scan", "seg_reduce", "seg_block_sum", "seg_finalize"]
 
 

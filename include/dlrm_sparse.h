@@ -53,13 +53,16 @@ enum dlrm_status {
     DLRM_ERR_INDEX_OOB = -4,
     DLRM_ERR_BAD_OFFSETS = -5,
     DLRM_ERR_CAPACITY = -6,
-    DLRM_ERR_CUDA = -7
+    DLRM_ERR_CUDA = -7,
+    DLRM_ERR_WAIT_TIMEOUT = -8
 };
 
 /* Bits of the device error flag. */
 #define DLRM_FLAG_INDEX_OOB 1   /* an index was < 0 or >= rows of its table */
 #define DLRM_FLAG_BAD_OFFSETS 2 /* offsets not monotone, or not 0 .. nnz */
 #define DLRM_FLAG_CAPACITY 4    /* more unique rows than grad_rows can hold */
+#define DLRM_FLAG_WAIT_TIMEOUT 8 /* a kernel gave up waiting on another CTA's result
+                                    (every such wait is bounded); outputs invalid */
 
 #define DLRM_MAX_TABLES 256
 
@@ -176,7 +179,10 @@ size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d);
  * view           optional host struct, filled with device pointers to the
  *                integer results of the coalescing (see above).
  * nnz may be at most 2^31 and B at most 2^31 - 1 (DLRM_ERR_UNSUPPORTED
- * beyond); B == 0 requires nnz == 0.  The vectorised path needs d % 4 == 0,
+ * beyond); B == 0 requires nnz == 0.  The sort's CTAs wait on the results of
+ * earlier CTAs of the same launch, each wait bounded; one that runs out
+ * raises DLRM_FLAG_WAIT_TIMEOUT (results then invalid, all writes still
+ * inside the workspace and the tables' touched rows).  The vectorised path needs d % 4 == 0,
  * 16-byte aligned tables, dpooled and grad_rows, and dpooled strides that are
  * multiples of 4; other layouts take a scalar path.
  */

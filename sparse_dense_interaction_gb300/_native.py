@@ -18,8 +18,8 @@ from . import build as _build
 
 F32, F16, BF16 = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL = 0, -1, -2, -3
-ERR_INDEX_OOB, ERR_BAD_OFFSETS, ERR_CAPACITY, ERR_CUDA = -4, -5, -6, -7
-FLAG_INDEX_OOB, FLAG_BAD_OFFSETS, FLAG_CAPACITY = 1, 2, 4
+ERR_INDEX_OOB, ERR_BAD_OFFSETS, ERR_CAPACITY, ERR_CUDA, ERR_WAIT_TIMEOUT = -4, -5, -6, -7, -8
+FLAG_INDEX_OOB, FLAG_BAD_OFFSETS, FLAG_CAPACITY, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
 MAX_TABLES = 256
 
 _TORCH_DTYPES = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}

@@ -223,6 +223,8 @@ int dlrm_read_error(const int32_t *err_flag, dlrm_stream_t stream)
         return DLRM_ERR_BAD_OFFSETS;
     if (h & DLRM_FLAG_CAPACITY)
         return DLRM_ERR_CAPACITY;
+    if (h & DLRM_FLAG_WAIT_TIMEOUT)
+        return DLRM_ERR_WAIT_TIMEOUT;
     return DLRM_OK;
 }
 
@@ -254,6 +256,8 @@ const char *dlrm_status_string(int status)
         return "more unique rows than grad_rows can hold";
     case DLRM_ERR_CUDA:
         return "CUDA error";
+    case DLRM_ERR_WAIT_TIMEOUT:
+        return "a kernel's bounded wait on another CTA ran out";
     default:
         return "unknown status";
     }

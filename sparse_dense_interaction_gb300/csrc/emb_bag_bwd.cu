@@ -12,10 +12,11 @@
 //  3. sort       stable LSD radix sort of (row, position) pairs, segmented by
 //                table: the CSR input is already grouped by table, so tiles
 //                never straddle a table and only the row bits are sorted
-//                (ceil(log2 max_rows) bits, <= 8 per pass).  Per pass:
-//                tile histograms -> per-(table,digit) scan across tiles ->
-//                stable local ranking in shared memory (warp match + per-warp
-//                histograms) and a coalesced scatter.
+//                (ceil(log2 max_rows) bits, <= 8 per pass).  One kernel
+//                counts the digits of every pass per table; then one kernel
+//                per pass ranks each tile in shared memory (warp match +
+//                per-warp histograms), finds the counts of the tiles before
+//                it by decoupled look-back, and scatters coalesced.
 //  4. count      run starts (a new row, or a table's first lookup) per tile
 //  5. scan       exclusive scan of the per-tile counts: the runs' unique ids
 //  6. reduce     per tile, the summed pooled gradient of every run of equal
@@ -26,7 +27,7 @@
 namespace dlrm {
 
 struct BwdLayout {
-    size_t keys[2], vals[2], bag_of, uniq_table, uniq_row, seg_off, hist, counts, tstart, tile_base,
+    size_t keys[2], vals[2], bag_of, uniq_table, uniq_row, seg_off, status[2], tile_ctr, tile_hist, counts, tstart, tile_base,
         tile_count, tile_ubase, chunk_flags, chunk_tail_u, head, tail, block_flags, block_sum, num_unique, total;
     int64_t ntiles_max, nchunks_max;
 };
@@ -53,7 +54,10 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.uniq_table = take(n4);
     L.uniq_row = take(n4);
     L.seg_off = take(n4 + 4);
-    L.hist = take((size_t)kRadix * L.ntiles_max * 4);
+    L.status[0] = take((size_t)kRadix * L.ntiles_max * 8);
+    L.status[1] = take((size_t)kRadix * L.ntiles_max * 8);
+    L.tile_ctr = take((size_t)kMaxPasses * 4);
+    L.tile_hist = take((size_t)L.ntiles_max * 2 * kMaxPasses * kRadix * 4);
     L.counts = take((size_t)kMaxPasses * T * kRadix * 4);
     L.tstart = take(((size_t)T + 1) * 4);
     L.tile_base = take(((size_t)T + 1) * 4);
@@ -107,8 +111,8 @@ bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t n
     __syncthreads();
     for (int t = threadIdx.x; t <= T; t += blockDim.x)
         w.tstart[t] = (uint32_t)start[t];
-    for (int i = threadIdx.x; i < kMaxPasses * T * kRadix; i += blockDim.x)
-        w.counts[i] = 0;
+    if (threadIdx.x < kMaxPasses)
+        w.tile_ctr[threadIdx.x] = 0;
 }
 
 // ------------------------------------------------------------- bag ids ---
@@ -166,96 +170,146 @@ __device__ __forceinline__ uint32_t pass0_key(const int64_t *indices, uint32_t j
     return (r >= 0 && r < R) ? (uint32_t)r : kSentinel;
 }
 
-__global__ void __launch_bounds__(kSortThreads)
-sort_upsweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__ indices,
-                    TableSet ts, int T, BwdPtrs w, int32_t *err)
+// Digit width and shift of pass p when `bits` key bits are split over
+// `passes` passes as evenly as possible (wider passes first).
+__host__ __device__ __forceinline__ int pass_bits(int bits, int passes, int p)
 {
-    __shared__ uint32_t hist[kRadix];
+    return bits / passes + (p < bits % passes ? 1 : 0);
+}
+
+// Digit counts of every pass from one read of the indices, per half tile
+// (two CTAs per tile), written to the tile's row of counts.  A table's digit
+// histogram does not depend on the order of its keys, so all passes are
+// counted here; the digit scan below sums the rows of the table's tiles, and
+// each pass finds the counts of the tiles before its own by looking back.
+// Also clears the look-back words of pass 0 and flags indices out of range.
+constexpr int kHistItems = kItems / 2;
+__global__ void __launch_bounds__(kSortThreads)
+sort_hist_kernel(int bits, int passes, const int64_t *__restrict__ indices, TableSet ts, int T, BwdPtrs w,
+                 int32_t *err)
+{
+    static_assert(kSortThreads == kRadix, "one thread per digit");
+    __shared__ uint32_t h[kMaxPasses][kRadix];
     __shared__ TileInfo ti;
-    if (threadIdx.x == 0)
-        find_tile(blockIdx.x, T, w.tile_base, w.tstart, ti);
-    for (int i = threadIdx.x; i < kRadix; i += blockDim.x)
-        hist[i] = 0;
+    const int tid = threadIdx.x;
+    const int64_t tau = blockIdx.x >> 1;
+    const int half = blockIdx.x & 1;
+    if (tid == 0)
+        find_tile(tau, T, w.tile_base, w.tstart, ti);
+    for (int i = tid; i < kMaxPasses * kRadix; i += kSortThreads)
+        (&h[0][0])[i] = 0;
     __syncthreads();
     if (!ti.valid)
         return;
-    const uint32_t mask = (1u << nbits) - 1u;
-    // pass p reads buffer (p+1)&1 (written by pass p-1) and writes buffer p&1
-    const uint32_t *keys = w.keys[(pass + 1) & 1];
+    if (tid < kRadix / 2)
+        w.status[0][(size_t)tau * kRadix + half * (kRadix / 2) + tid] = 0;
     const int64_t R = ts.rows[ti.t];
+    const uint32_t lo = ti.lo + half * (kTile / 2);
+    uint32_t key[kHistItems];
+#pragma unroll
+    for (int i = 0; i < kHistItems; i++) {
+        const uint32_t j = lo + i * kSortThreads + tid;
+        key[i] = j < ti.hi ? pass0_key(indices, j, R) : 0u;
+    }
     bool oob = false;
-    const int lane = threadIdx.x & 31;
-    for (uint32_t base = ti.lo; base < ti.hi; base += kSortThreads) {
-        const uint32_t j = base + threadIdx.x;
-        const bool valid = j < ti.hi;
-        uint32_t digit = kRadix;  // never matches a real digit
-        if (valid) {
-            uint32_t key;
-            if (pass == 0) {
-                key = pass0_key(indices, j, R);
-                oob |= key == kSentinel;
-            } else {
-                key = keys[j];
+#pragma unroll
+    for (int i = 0; i < kHistItems; i++) {
+        if (lo + i * kSortThreads + tid < ti.hi) {
+            oob |= key[i] == kSentinel;
+            int shift = 0;
+            for (int p = 0; p < passes; p++) {
+                const int nb = pass_bits(bits, passes, p);
+                atomicAdd(&h[p][(key[i] >> shift) & ((1u << nb) - 1u)], 1u);
+                shift += nb;
             }
-            digit = (key >> shift) & mask;
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, digit);
-        if (valid && lane == __ffs(peers) - 1)
-            atomicAdd(&hist[digit], __popc(peers));
     }
     if (oob)
         raise_flag(err, DLRM_FLAG_INDEX_OOB);
     __syncthreads();
-    uint32_t *counts = w.counts + ((size_t)pass * T + ti.t) * kRadix;
-    for (int dg = threadIdx.x; dg <= (int)mask; dg += blockDim.x) {
-        const uint32_t c = hist[dg];
-        w.hist[(size_t)dg * w.ntiles_max + blockIdx.x] = c;
-        if (c)
-            atomicAdd(&counts[dg], c);
-    }
+    uint32_t *row = w.tile_hist + ((size_t)blockIdx.x * kMaxPasses) * kRadix;
+    for (int p = 0; p < passes; p++)
+        row[p * kRadix + tid] = h[p][tid];
 }
 
-// One warp per (table, digit): global start of the digit's run in the table
-// plus the exclusive prefix over the table's tiles, written in place.
-__global__ void __launch_bounds__(256)
-sort_scan_kernel(int pass, int nbits, int T, BwdPtrs w)
+// One CTA per (pass, table): sums the digit counts of the table's half tiles
+// (four groups of kRadix threads, one thread per digit, each over every
+// fourth row) and scans them into the start position of each digit's keys in
+// the table's sorted range.
+constexpr int kScanGroups = 4;
+__global__ void __launch_bounds__(kScanGroups * kRadix)
+sort_digit_scan_kernel(int passes, int T, BwdPtrs w)
 {
-    const int radix = 1 << nbits;
-    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (gw >= (int64_t)T * radix)
-        return;
-    const int t = (int)(gw / radix);
-    const int dg = (int)(gw % radix);
-    const uint32_t *counts = w.counts + ((size_t)pass * T + t) * kRadix;
-    uint32_t below = 0;
-    for (int i = lane; i < dg; i += 32)
-        below += counts[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        below += __shfl_xor_sync(0xffffffffu, below, o);
-    uint32_t run = w.tstart[t] + below;
-    const uint32_t t0 = w.tile_base[t], t1 = w.tile_base[t + 1];
-    uint32_t *h = w.hist + (size_t)dg * w.ntiles_max;
-    for (uint32_t tb = t0; tb < t1; tb += 32) {
-        const uint32_t tau = tb + lane;
-        const uint32_t v = tau < t1 ? h[tau] : 0u;
-        uint32_t incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o)
-                incl += n;
-        }
-        if (tau < t1)
-            h[tau] = run + incl - v;
-        run += __shfl_sync(0xffffffffu, incl, 31);
+    __shared__ uint32_t part[kScanGroups][kRadix];
+    __shared__ uint32_t wsum[kRadix / 32];
+    const int p = blockIdx.x / T, t = blockIdx.x % T;
+    const int tid = threadIdx.x, dg = tid % kRadix, g = tid / kRadix, lane = tid & 31, warp = tid >> 5;
+    const uint32_t h0 = 2 * w.tile_base[t], h1 = 2 * w.tile_base[t + 1];
+    const uint32_t *col = w.tile_hist + (size_t)p * kRadix + dg;
+    constexpr size_t kRow = (size_t)kMaxPasses * kRadix;  // words per half tile
+    uint32_t c = 0;
+    uint32_t hb = h0 + g;
+    for (; hb + 3 * kScanGroups < h1; hb += 4 * kScanGroups) {
+        const uint32_t a0 = col[hb * kRow], a1 = col[(hb + kScanGroups) * kRow];
+        const uint32_t a2 = col[(hb + 2 * kScanGroups) * kRow], a3 = col[(hb + 3 * kScanGroups) * kRow];
+        c += (a0 + a1) + (a2 + a3);
     }
+    for (; hb < h1; hb += kScanGroups)
+        c += col[hb * kRow];
+    part[g][dg] = c;
+    __syncthreads();
+    if (tid >= kRadix)
+        return;
+    c = 0;
+#pragma unroll
+    for (int gi = 0; gi < kScanGroups; gi++)
+        c += part[gi][dg];
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += x;
+    }
+    if (lane == 31)
+        wsum[warp] = incl;
+    // named barrier over the first kRadix threads only (the rest have left)
+    asm volatile("bar.sync 1, %0;" ::"n"(kRadix));
+    uint32_t before = 0;
+    for (int wi = 0; wi < warp; wi++)
+        before += wsum[wi];
+    w.counts[((size_t)p * T + t) * kRadix + dg] = w.tstart[t] + before + incl - c;
 }
 
-__global__ void __launch_bounds__(kSortThreads)
-sort_downsweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__ indices,
-                      TableSet ts, int T, BwdPtrs w)
+// Look-back words: kind in the high half (0 = not yet written), count in the
+// low half.  Each word is written whole, so a reader sees a kind with its own
+// count and needs no other ordering.
+constexpr uint32_t kAggregate = 1u;  // the tile's own count of the digit
+constexpr uint32_t kInclusive = 2u;  // count of the digit in this and all earlier tiles of the table
+constexpr int kSpinLimit = 1 << 20;  // polls of one word before a wait gives up (about a second)
+
+__device__ __forceinline__ void store_status(uint64_t *p, uint32_t kind, uint32_t count)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(((uint64_t)kind << 32) | count) : "memory");
+}
+
+__device__ __forceinline__ uint64_t load_status(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// One radix pass in a single launch.  Tiles are taken in order from a
+// counter, so every tile before a CTA's own is held by a CTA that is running
+// or done; the CTA ranks its keys in shared memory, publishes its digit
+// counts, sums the counts of the tiles before it in the same table (decoupled
+// look-back), and scatters its keys, in stable order, to the digit ranges
+// found by the histogram kernel.  A wait that runs out raises
+// DLRM_FLAG_WAIT_TIMEOUT and writes stay inside the table's range.
+__global__ void __launch_bounds__(kSortThreads, 4)
+sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__ indices, TableSet ts, int T,
+                     BwdPtrs w, int32_t *err)
 {
     __shared__ uint32_t skey[kTile];
     __shared__ uint32_t sval[kTile];
@@ -264,37 +318,40 @@ sort_downsweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict_
     __shared__ uint32_t gbase[kRadix];
     __shared__ uint32_t wsum[8];
     __shared__ TileInfo ti;
+    __shared__ uint32_t tau_s;
+    __shared__ int timed_out;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0)
-        find_tile(blockIdx.x, T, w.tile_base, w.tstart, ti);
+    if (tid == 0) {
+        tau_s = atomicAdd(&w.tile_ctr[pass], 1u);
+        find_tile(tau_s, T, w.tile_base, w.tstart, ti);
+        timed_out = 0;
+    }
     for (int i = tid; i < 8 * kRadix; i += kSortThreads)
         (&whist[0][0])[i] = 0;
     __syncthreads();
     if (!ti.valid)
         return;
+    const uint32_t tau = tau_s;
+    // the next pass reuses the other buffer of look-back words: clear this tile's
+    w.status[(pass + 1) & 1][(size_t)tau * kRadix + tid] = 0;
     const uint32_t mask = (1u << nbits) - 1u;
     const int radix = 1 << nbits;
-    for (int dg = tid; dg < radix; dg += kSortThreads)
-        gbase[dg] = w.hist[(size_t)dg * w.ntiles_max + blockIdx.x];
     const uint32_t *keys_in = w.keys[(pass + 1) & 1];
     const uint32_t *vals_in = w.vals[(pass + 1) & 1];
     uint32_t *keys_out = w.keys[pass & 1];
     uint32_t *vals_out = w.vals[pass & 1];
     const int64_t R = ts.rows[ti.t];
 
-    uint32_t key[kItems], val[kItems], rank[kItems];
+    uint32_t key[kItems], rank[kItems];  // values are read at the local scatter
     const uint32_t wbase = ti.lo + warp * (kTile / 8);
 #pragma unroll
     for (int i = 0; i < kItems; i++) {
         const uint32_t j = wbase + i * 32 + lane;
         const bool valid = j < ti.hi;
-        if (pass == 0) {
+        if (pass == 0)
             key[i] = valid ? pass0_key(indices, j, R) : 0u;
-            val[i] = j;
-        } else {
+        else
             key[i] = valid ? keys_in[j] : 0u;
-            val[i] = valid ? vals_in[j] : 0u;
-        }
     }
     // stable rank within the warp: items in position order (i, then lane)
 #pragma unroll
@@ -314,7 +371,7 @@ sort_downsweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict_
         rank[i] = r;
     }
     __syncthreads();
-    // per digit: exclusive prefix across warps, then across digits
+    // per digit: exclusive prefix across warps and the tile's total
     uint32_t total = 0;
     if (tid < radix) {
         for (int wi = 0; wi < 8; wi++) {
@@ -323,6 +380,11 @@ sort_downsweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict_
             total += c;
         }
     }
+    const uint32_t t0 = w.tile_base[ti.t];  // the table's first tile
+    const bool first = tau == t0;
+    uint64_t *stat = w.status[pass & 1];
+    if (tid < radix)
+        store_status(stat + (size_t)tau * kRadix + tid, first ? kInclusive : kAggregate, total);
     // block-wide exclusive scan of the digit totals (radix <= 256 threads)
     uint32_t incl = total;
 #pragma unroll
@@ -347,17 +409,48 @@ sort_downsweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict_
             const uint32_t digit = (key[i] >> shift) & mask;
             const uint32_t lp = tdig[digit] + whist[warp][digit] + rank[i];
             skey[lp] = key[i];
-            sval[lp] = val[i];
+            sval[lp] = pass == 0 ? j : vals_in[j];
         }
     }
+    // look back over the tiles before this one in the table (after the local
+    // scatter, so that they have had the longest time to publish)
+    if (tid < radix) {
+        uint32_t excl = 0;
+        if (!first) {
+            uint32_t k = tau - 1;
+            int spins = 0;
+            for (;;) {
+                const uint64_t v = load_status(stat + (size_t)k * kRadix + tid);
+                const uint32_t kind = (uint32_t)(v >> 32);
+                if (kind == 0u) {
+                    if (++spins > kSpinLimit) {
+                        timed_out = 1;
+                        break;
+                    }
+                    continue;
+                }
+                excl += (uint32_t)v;
+                if (kind == kInclusive || k == t0)
+                    break;
+                k--;
+            }
+            store_status(stat + (size_t)tau * kRadix + tid, kInclusive, excl + total);
+        }
+        gbase[tid] = w.counts[((size_t)pass * T + ti.t) * kRadix + tid] + excl;
+    }
     __syncthreads();
+    if (tid == 0 && timed_out)
+        raise_flag(err, DLRM_FLAG_WAIT_TIMEOUT);
     const uint32_t n = ti.hi - ti.lo;
+    const uint32_t tbeg = w.tstart[ti.t], tlen = w.tstart[ti.t + 1] - tbeg;
     for (uint32_t j = tid; j < n; j += kSortThreads) {
         const uint32_t k = skey[j];
         const uint32_t digit = (k >> shift) & mask;
         const uint32_t dest = gbase[digit] + (j - tdig[digit]);
-        keys_out[dest] = k;
-        vals_out[dest] = sval[j];
+        if (dest - tbeg < tlen) {
+            keys_out[dest] = k;
+            vals_out[dest] = sval[j];
+        }
     }
 }
 
@@ -502,7 +595,10 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
     w.uniq_table = reinterpret_cast<int32_t *>(base + L.uniq_table);
     w.uniq_row = reinterpret_cast<uint32_t *>(base + L.uniq_row);
     w.seg_off = reinterpret_cast<uint32_t *>(base + L.seg_off);
-    w.hist = reinterpret_cast<uint32_t *>(base + L.hist);
+    w.status[0] = reinterpret_cast<uint64_t *>(base + L.status[0]);
+    w.status[1] = reinterpret_cast<uint64_t *>(base + L.status[1]);
+    w.tile_ctr = reinterpret_cast<uint32_t *>(base + L.tile_ctr);
+    w.tile_hist = reinterpret_cast<uint32_t *>(base + L.tile_hist);
     w.counts = reinterpret_cast<uint32_t *>(base + L.counts);
     w.tstart = reinterpret_cast<uint32_t *>(base + L.tstart);
     w.tile_base = reinterpret_cast<uint32_t *>(base + L.tile_base);
@@ -548,19 +644,18 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
             return s;
     }
     const int64_t grid = L.ntiles_max;
+    sort_hist_kernel<<<(unsigned)(2 * grid), kSortThreads, 0, st>>>(bits, passes, indices, ts, T, w, err);
+    count_launch(st);
+    if ((s = launch_status()) != DLRM_OK)
+        return s;
+    sort_digit_scan_kernel<<<(unsigned)(passes * T), kScanGroups * kRadix, 0, st>>>(passes, T, w);
+    count_launch(st);
+    if ((s = launch_status()) != DLRM_OK)
+        return s;
     int shift = 0;
     for (int p = 0; p < passes; p++) {
-        const int nb = bits / passes + (p < bits % passes ? 1 : 0);
-        sort_upsweep_kernel<<<(unsigned)grid, kSortThreads, 0, st>>>(p, shift, nb, indices, ts, T, w, err);
-        count_launch(st);
-        if ((s = launch_status()) != DLRM_OK)
-            return s;
-        const int64_t warps = (int64_t)T << nb;
-        sort_scan_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(p, nb, T, w);
-        count_launch(st);
-        if ((s = launch_status()) != DLRM_OK)
-            return s;
-        sort_downsweep_kernel<<<(unsigned)grid, kSortThreads, 0, st>>>(p, shift, nb, indices, ts, T, w);
+        const int nb = pass_bits(bits, passes, p);
+        sort_onesweep_kernel<<<(unsigned)grid, kSortThreads, 0, st>>>(p, shift, nb, indices, ts, T, w, err);
         count_launch(st);
         if ((s = launch_status()) != DLRM_OK)
             return s;
