@@ -137,6 +137,34 @@ int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb,
                       float *demb, int64_t demb_sample_stride, dlrm_stream_t stream);
 
 /*
+ * Embedding-bag forward and interaction forward in one call ("Notes/DLRM",
+ * section 3: the interaction directly follows the lookups).  Computes what
+ * dlrm_emb_bag_fwd followed by dlrm_interact_fwd with N = T computes:
+ *
+ *   pooled[b][t] = sum_{k in bag (t,b)} tables[t][indices[k]]      (fp32)
+ *   y[b]         = [ e0[b] | z_i . z_j over the pairs (i, j) ]     (z_0 = e0[b],
+ *                                                                   z_i = pooled[b][i-1])
+ *
+ * without writing the pooled block unless `pooled` is given (the backward
+ * needs it; inference does not).  Arguments as in those two calls; pooled is
+ * optional (NULL: not written), with strides in elements.  The pooled values
+ * equal dlrm_emb_bag_fwd's bit for bit; y equals dlrm_interact_fwd's within
+ * fp32 rounding (its dot products add their columns in another order).
+ * T may be 1 .. 127.  The single-kernel path needs rows of a whole number of
+ * 16-byte chunks up to 1 KB, 16-byte aligned tables (and pooled, with
+ * strides that are multiples of 4), and a Z block of each sample that fits
+ * on chip (about (T + 1) <= 32 with d <= 256); otherwise the call runs the
+ * two kernels through `pooled`, which must then be given with
+ * pooled_table_stride == d, else DLRM_ERR_UNSUPPORTED.  Errors are flagged
+ * as in dlrm_emb_bag_fwd.
+ */
+int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                              const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                              const float *e0, int64_t e0_stride, int include_self, float *y,
+                              int64_t y_stride, float *pooled, int64_t pooled_sample_stride,
+                              int64_t pooled_table_stride, int32_t *err_flag, dlrm_stream_t stream);
+
+/*
  * Device pointers into the workspace of the last dlrm_emb_bag_bwd_sgd call,
  * valid once the stream has passed that call and until the workspace is
  * reused.  The coalescing is a stable sort of lookup positions by

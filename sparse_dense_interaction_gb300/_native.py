@@ -48,6 +48,8 @@ SIGNATURES = {
     "dlrm_emb_bag_bwd_sgd_noalloc": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp,
                                             _i64, _i64, _f32, _vp, _i64, ctypes.POINTER(CoalescedView),
                                             _vp, _vp]),
+    "dlrm_emb_bag_interact_fwd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64, _i32,
+                                         _vp, _i64, _vp, _i64, _i64, _vp, _vp]),
     "dlrm_read_error": (_i32, [_vp, _vp]),
     "dlrm_clear_error": (_i32, [_vp, _vp]),
     "dlrm_status_string": (ctypes.c_char_p, [_i32]),
@@ -194,6 +196,27 @@ def dlrm_emb_bag_bwd_sgd(tables, offsets, indices, B: int, dpooled, lr: float, w
                 uniq_row=sub(view.uniq_row, nnz, torch.int32),
                 seg_off=sub(view.seg_off, nnz + 1, torch.int32),
                 num_unique=sub(view.num_unique, 1, torch.int64))
+
+
+def dlrm_emb_bag_interact_fwd(tables, offsets, indices, B: int, e0, include_self: bool, y, pooled=None,
+                              err_flag=None, stream=None):
+    """Lookup + interaction forward in one call: ``y`` ([B][d + P] fp32, last
+    dim 1) receives what :func:`dlrm_interact_fwd` would give on the pooled
+    vectors of :func:`dlrm_emb_bag_fwd`; ``pooled`` ([B][T][d] fp32, optional)
+    also receives those pooled vectors."""
+    ptrs, rows, T, d, dtype = _tables(tables)
+    if e0.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("e0 and y must have unit stride in their last dimension")
+    pss = pts = 0
+    if pooled is not None:
+        if pooled.stride(2) != 1:
+            raise ValueError("pooled must have unit stride in its last dimension")
+        pss, pts = pooled.stride(0), pooled.stride(1)
+    _check(load().dlrm_emb_bag_interact_fwd(ptrs, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices),
+                                            indices.numel(), B, e0.data_ptr(), e0.stride(0),
+                                            1 if include_self else 0, y.data_ptr(), y.stride(0), _ptr(pooled),
+                                            pss, pts, _ptr(err_flag), _stream(stream)),
+           "dlrm_emb_bag_interact_fwd")
 
 
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024

@@ -41,6 +41,14 @@ int launch_interact_fwd(const float *, int64_t, const float *, int64_t, int, int
                         int64_t, cudaStream_t);
 int launch_interact_bwd(const float *, int64_t, const float *, int64_t, int, int, int64_t, int,
                         const float *, int64_t, float *, int64_t, float *, int64_t, cudaStream_t);
+struct FusedShape {
+    int S, KS, threads;
+    size_t smem;
+};
+bool emb_bag_interact_shape(int, int, int, int64_t, FusedShape &);
+int launch_emb_bag_interact_fwd(const TableSet &, int, int, int, const int64_t *, const int64_t *, int64_t,
+                                int64_t, const float *, int64_t, int, float *, int64_t, float *, int64_t, int64_t,
+                                const FusedShape &, int32_t *, cudaStream_t);
 bool emb_bag_bwd_vectorisable(const TableSet &, int, int, const float *, int64_t, int64_t, const float *);
 size_t emb_bag_bwd_workspace(int, int64_t, int);
 int launch_emb_bag_bwd(const TableSet &, int, int, int, const int64_t *, const int64_t *, int64_t, int64_t,
@@ -165,6 +173,54 @@ int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb, int6
     return launch_interact_bwd(e0, e0_stride, emb, emb_sample_stride, N, d, B, include_self ? 1 : 0, dy,
                                dy_stride, de0, de0_stride, demb, demb_sample_stride,
                                static_cast<cudaStream_t>(stream));
+}
+
+int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                              const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                              const float *e0, int64_t e0_stride, int include_self, float *y, int64_t y_stride,
+                              float *pooled, int64_t pooled_sample_stride, int64_t pooled_table_stride,
+                              int32_t *err_flag, dlrm_stream_t stream)
+{
+    TableSet ts;
+    int s = make_tables(tables, rows, T, d, dtype, ts);
+    if (s != DLRM_OK)
+        return s;
+    if (B < 0 || nnz < 0 || e0_stride < d || y_stride < d + dlrm_num_pairs(T, include_self))
+        return DLRM_ERR_INVALID_ARG;
+    if (pooled && (pooled_sample_stride < 0 || pooled_table_stride < 0))
+        return DLRM_ERR_INVALID_ARG;
+    if (T > 127 || B > (int64_t)1 << 31)
+        return DLRM_ERR_UNSUPPORTED;
+    if (B == 0)
+        return DLRM_OK;
+    if (!offsets || !e0 || !y || (nnz > 0 && !indices))
+        return DLRM_ERR_INVALID_ARG;
+    if (!aligned(offsets, 8) || (indices && !aligned(indices, 8)) || !aligned(e0, 4) || !aligned(y, 4) ||
+        (pooled && !aligned(pooled, 4)))
+        return DLRM_ERR_INVALID_ARG;
+    const int inc = include_self ? 1 : 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t row_bytes = (int64_t)d * elem_bytes(dtype);
+    bool fused = row_bytes % 16 == 0 && row_bytes <= 1024;
+    for (int t = 0; t < T && fused; t++)
+        fused = aligned(tables[t], 16);
+    if (pooled)
+        fused = fused && aligned(pooled, 16) && pooled_sample_stride % 4 == 0 && pooled_table_stride % 4 == 0;
+    FusedShape fs;
+    if (fused && emb_bag_interact_shape(T, d, inc, B, fs))
+        return launch_emb_bag_interact_fwd(ts, T, d, dtype, offsets, indices, nnz, B, e0, e0_stride, inc, y,
+                                           y_stride, pooled, pooled_sample_stride, pooled_table_stride, fs,
+                                           err_flag, st);
+    // the two calls it fuses, through the caller's pooled block
+    if (!pooled || pooled_table_stride != d)
+        return DLRM_ERR_UNSUPPORTED;
+    const bool vec = emb_bag_fwd_vectorisable(ts, T, d, elem_bytes(dtype), pooled, pooled_sample_stride,
+                                              pooled_table_stride);
+    s = launch_emb_bag_fwd(ts, T, d, dtype, vec, offsets, indices, nnz, B, pooled, pooled_sample_stride,
+                           pooled_table_stride, err_flag, st);
+    if (s != DLRM_OK)
+        return s;
+    return launch_interact_fwd(e0, e0_stride, pooled, pooled_sample_stride, T, d, B, inc, y, y_stride, st);
 }
 
 size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d)

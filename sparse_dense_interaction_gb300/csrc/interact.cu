@@ -23,16 +23,9 @@
 // F rows of the chunk (a broadcast 16-byte load of four G entries and a
 // conflict-free 16-byte load of four Z entries per 16 FMAs).  dZ rows go
 // straight to de0 (plus the e0 part of dy) and to the pooled gradients.
-#include "common.cuh"
+#include "interact.cuh"
 
 namespace dlrm {
-
-constexpr int kKC = 32;  // columns of Z per shared-memory chunk
-
-__device__ __forceinline__ int64_t pair_pos(int i, int j, int inc)
-{
-    return inc ? (int64_t)i * (i + 1) / 2 + j : (int64_t)i * (i - 1) / 2 + j;
-}
 
 // 8 consecutive fp32 values of a row, zero past the end (d) or past B.
 __device__ __forceinline__ void load8(const float *src, int k, int d, bool vec, float *v)
@@ -47,15 +40,6 @@ __device__ __forceinline__ void load8(const float *src, int k, int d, bool vec, 
         for (int m = 0; m < 8; m++)
             v[m] = (k + m < d) ? __ldg(src + k + m) : 0.f;
     }
-}
-
-// Position of element (k, i) in a staged row of TS columns (TS a multiple
-// of 32): 4-column groups are XOR-swizzled by bits 3..4 of k, so the
-// transposing stores of 8 rows x 4 column octets from one warp hit 32
-// distinct banks, while 4 consecutive columns stay one aligned 16-byte word.
-__device__ __forceinline__ int zt_col(int k, int i)
-{
-    return ((((i >> 2) ^ (((k >> 3) & 3) << 1))) << 2) | (i & 3);
 }
 
 __global__ void __launch_bounds__(1024)
@@ -77,13 +61,7 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
     const int tid = threadIdx.x;
     const int64_t b0 = (int64_t)blockIdx.x * S;
 
-    for (int idx = tid; idx < ntiles; idx += blockDim.x) {
-        int I = 0;
-        while ((I + 1) * (I + 2) / 2 <= idx)
-            I++;
-        tileI[idx] = (uint8_t)I;
-        tileJ[idx] = (uint8_t)(idx - I * (I + 1) / 2);
-    }
+    fill_tile_tables(ntiles, tileI, tileJ);
 
     const int s = tid / ntiles;
     const int tile = tid - s * ntiles;
@@ -293,11 +271,6 @@ interact_bwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
         }
         __syncthreads();
     }
-}
-
-static inline int64_t num_pairs_of(int F, int inc)
-{
-    return inc ? (int64_t)F * (F + 1) / 2 : (int64_t)F * (F - 1) / 2;
 }
 
 static bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }

@@ -105,6 +105,24 @@ def test_interaction_rejects_bad_arguments(lib):
     assert lib.dlrm_kernel_launch_count() == 0
 
 
+def test_fused_forward_rejects_bad_arguments(lib):
+    p, r = _tables(4)
+    width = 16 + 10  # d + P for F = 5 strict
+    call = lambda **kw: lib.dlrm_emb_bag_interact_fwd(
+        kw.get("tables", p), kw.get("rows", r), kw.get("T", 4), 16, 0, FAKE, FAKE, 10, kw.get("B", 2),
+        kw.get("e0", FAKE), kw.get("e0s", 16), 0, kw.get("y", FAKE), kw.get("ys", width),
+        kw.get("pooled", None), kw.get("pss", 64), 16, None, None)
+    assert call(ys=width - 1) == _native.ERR_INVALID_ARG
+    assert call(e0s=15) == _native.ERR_INVALID_ARG
+    assert call(e0=None) == _native.ERR_INVALID_ARG
+    assert call(y=None) == _native.ERR_INVALID_ARG
+    assert call(pooled=FAKE, pss=-1) == _native.ERR_INVALID_ARG
+    big_p, big_r = _tables(128)
+    assert call(tables=big_p, rows=big_r, T=128, ys=100000) == _native.ERR_UNSUPPORTED  # N <= 127
+    assert call(B=0) == _native.OK
+    assert lib.dlrm_kernel_launch_count() == 0
+
+
 def test_backward_rejects_bad_arguments(lib):
     p, r = _tables(2)
     need = sdi.dlrm_emb_bag_bwd_workspace_size(2, 8, 100, 16)
