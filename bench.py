@@ -57,6 +57,10 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--schedule", choices=["overlap", "serial"], default="overlap",
+                   help="overlap: the backward's coalescing runs on a side stream next to the forward")
+    p.add_argument("--fwd", choices=["separate", "fused"], default="separate",
+                   help="fused: one kernel for the lookup and the interaction forward")
     p.add_argument("--batch", type=int, default=None, help="override the batch size (profiling runs)")
     p.add_argument("--tables", type=int, default=None, help="override the table count (profiling runs)")
     p.add_argument("--rows", type=int, default=None, help="override the rows per table (profiling runs)")
@@ -175,7 +179,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(cfg),
+        "config": dict(config_of(cfg), schedule=args.schedule, forward=args.fwd),
         "cpu_baseline": {"value": value, "unit": "samples/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -262,7 +266,7 @@ class ClockSampler:
 class Step:
     """Device buffers and the launches of one step of the path."""
 
-    def __init__(self, cfg, seed, dev):
+    def __init__(self, cfg, seed, dev, schedule="overlap", fwd="separate"):
         import torch
 
         import sparse_dense_interaction_gb300 as sdi
@@ -288,27 +292,55 @@ class Step:
                               device=dev)
         self.grad = torch.empty((self.nnz, d), device=dev) if cfg["update"] == "grad" else None
         self.flag = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.schedule, self.fwd = schedule, fwd
+        self.side = torch.cuda.Stream(dev)
+        self.coalesced = torch.cuda.Event()
 
     def run(self, prof=None):
-        """One step; with `prof`, a list that receives (kernel name, start event, end event)."""
-        sdi, c = self.sdi, self.cfg
-        calls = [("emb_bag_fwd", lambda: sdi.dlrm_emb_bag_fwd(self.tables, self.offsets, self.indices,
-                                                                c["B"], self.pooled, err_flag=self.flag))]
-        if self.inter:
-            calls.append(("interact_fwd", lambda: sdi.dlrm_interact_fwd(self.e0, self.pooled,
-                                                                        c["include_self"], self.y)))
-            calls.append(("interact_bwd", lambda: sdi.dlrm_interact_bwd(
-                self.e0, self.pooled, c["include_self"], self.dy, self.de0, self.dpooled)))
-        calls.append(("emb_bag_bwd", lambda: sdi.dlrm_emb_bag_bwd_sgd(
-            self.tables, self.offsets, self.indices, c["B"], self.dpooled, c["lr"], self.ws,
-            grad_rows=self.grad, err_flag=self.flag)))
-        for name, fn in calls:
+        """One step: lookup, interaction forward and backward, lookup backward with the
+        update.  With the overlapped schedule the backward's coalescing (which needs
+        only the indices) runs on a side stream next to the forward kernels, and the
+        reduce waits for it.  With `prof`, every library kernel is bracketed by events."""
+        sdi, c, torch = self.sdi, self.cfg, self.torch
+        main = torch.cuda.current_stream(self.dev)
+
+        def call(name, fn, stream):
             if prof is None:
                 fn()
             else:
-                prof.begin(name)
+                prof.begin(name, stream)
                 fn()
                 prof.end()
+
+        if self.schedule == "overlap":
+            self.side.wait_stream(main)  # this step's inputs, the previous step's reduce
+            with torch.cuda.stream(self.side):
+                call("coalesce", lambda: sdi.dlrm_emb_bag_coalesce(
+                    c["rows"], c["d"], self.offsets, self.indices, c["B"], self.ws, err_flag=self.flag,
+                    stream=self.side), self.side)
+                self.coalesced.record(self.side)
+        if self.inter and self.fwd == "fused":
+            call("emb_bag_interact_fwd", lambda: sdi.dlrm_emb_bag_interact_fwd(
+                self.tables, self.offsets, self.indices, c["B"], self.e0, c["include_self"], self.y,
+                pooled=self.pooled, err_flag=self.flag), main)
+        else:
+            call("emb_bag_fwd", lambda: sdi.dlrm_emb_bag_fwd(self.tables, self.offsets, self.indices, c["B"],
+                                                             self.pooled, err_flag=self.flag), main)
+            if self.inter:
+                call("interact_fwd", lambda: sdi.dlrm_interact_fwd(self.e0, self.pooled, c["include_self"],
+                                                                   self.y), main)
+        if self.inter:
+            call("interact_bwd", lambda: sdi.dlrm_interact_bwd(
+                self.e0, self.pooled, c["include_self"], self.dy, self.de0, self.dpooled), main)
+        if self.schedule == "overlap":
+            main.wait_event(self.coalesced)
+            call("reduce_sgd", lambda: sdi.dlrm_emb_bag_reduce_sgd(
+                self.tables, self.nnz, c["B"], self.dpooled, c["lr"], self.ws, grad_rows=self.grad,
+                err_flag=self.flag), main)
+        else:
+            call("emb_bag_bwd", lambda: sdi.dlrm_emb_bag_bwd_sgd(
+                self.tables, self.offsets, self.indices, c["B"], self.dpooled, c["lr"], self.ws,
+                grad_rows=self.grad, err_flag=self.flag), main)
 
 
 class KernelProfiler:
@@ -320,7 +352,7 @@ class KernelProfiler:
         self.torch, self.sdi, self.stream = torch, sdi, stream
         self.pool = []
         self.calls = []  # (call name, start event, [events after each kernel])
-        n = n_steps * 4
+        n = n_steps * 5
         for _ in range(n):
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(max_per_call + 1)]
             for e in evs:
@@ -330,10 +362,10 @@ class KernelProfiler:
         self.next = 0
         self.cur = None
 
-    def begin(self, name):
+    def begin(self, name, stream=None):
         evs = self.pool[self.next]
         self.next += 1
-        evs[0].record(self.stream)
+        evs[0].record(stream if stream is not None else self.stream)
         self.sdi.dlrm_profile_events(evs[1:])
         self.cur = (name, evs, self.sdi.dlrm_kernel_launch_count())
 
@@ -355,10 +387,30 @@ class KernelProfiler:
 BWD_KERNELS_PREFIX = ["bwd_prep", "bag_ids"]
 
 
-def bwd_kernel_names(passes):
+def coalesce_kernel_names(passes):
     names = list(BWD_KERNELS_PREFIX) + ["sort_hist", "sort_digit_scan"]
     names += [f"sort_pass[{p}]" for p in range(passes)]
-    return names + ["seg_count", "seg_scan", "seg_reduce", "seg_block_sum", "seg_finalize"]
+    return names + ["seg_count", "seg_scan"]
+
+
+REDUCE_KERNELS = ["seg_reduce", "seg_block_sum", "seg_finalize"]
+
+
+def bwd_kernel_names(passes):
+    return coalesce_kernel_names(passes) + REDUCE_KERNELS
+
+
+def kernel_name(call, k, passes):
+    """Name of the k-th kernel that a library call launched."""
+    if call == "emb_bag_bwd":
+        return bwd_kernel_names(passes)[k]
+    if call == "coalesce":
+        return coalesce_kernel_names(passes)[k]
+    if call == "reduce_sgd":
+        return REDUCE_KERNELS[k]
+    if call == "emb_bag_interact_fwd" and k > 0:  # the two-kernel path of the fused call
+        return "interact_fwd"
+    return call
 
 
 def algorithmic_bytes(cfg, st):
@@ -376,6 +428,8 @@ def algorithmic_bytes(cfg, st):
     }
     if st.inter:
         width = d + st.P
+        # fused call: the lookup's reads, e0 in, y and the pooled block out
+        out["emb_bag_interact_fwd"] = out["emb_bag_fwd"] + B * d * 4 + B * width * 4
         out["interact_fwd"] = B * (T + 1) * d * 4 + B * width * 4
         out["interact_bwd"] = B * (T + 1) * d * 4 + B * width * 4 + B * (T + 1) * d * 4
     # the reduce + update kernel: sorted keys and positions, bag ids, the
@@ -405,7 +459,7 @@ def run_ours(args):
     sdi.load()
 
     cfg = workload_config(args)
-    st = Step(cfg, args.seed + rank, dev)
+    st = Step(cfg, args.seed + rank, dev, args.schedule, args.fwd)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         st.run()
@@ -444,7 +498,7 @@ def run_ours(args):
     passes = (bits + 7) // 8
     names = {}
     for (call, k) in per:
-        names[(call, k)] = bwd_kernel_names(passes)[k] if call == "emb_bag_bwd" else call
+        names[(call, k)] = kernel_name(call, k, passes)
     kernel_ms = {names[key]: float(np.mean(v)) for key, v in per.items()}
     alg, uniq = algorithmic_bytes(cfg, st)
     peak, peak_kind = measured_peaks()
@@ -461,7 +515,8 @@ def run_ours(args):
                 "algorithmic_bytes": alg[rl_kernel], "peak_source": peak_kind,
                 "kernel_ms": kernel_ms[rl_kernel]}
     es = W.ELEM_BYTES[cfg["dtype"]]
-    gathered = st.nnz * cfg["d"] * es / (kernel_ms["emb_bag_fwd"] / 1e3) / 1e9
+    fwd_key = "emb_bag_fwd" if "emb_bag_fwd" in kernel_ms else "emb_bag_interact_fwd"
+    gathered = st.nnz * cfg["d"] * es / (kernel_ms[fwd_key] / 1e3) / 1e9
 
     # end to end through the public API with host buffers
     e2e = e2e_measure(args, st, torch, sdi, stream, dev)
@@ -479,7 +534,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 accumulate, " + cfg["dtype"] + " tables",
             "data": "synthetic (seeded; Zipf/uniform indices, counter-hash tables)",
-            "config": config_of(cfg),
+            "config": dict(config_of(cfg), schedule=args.schedule, forward=args.fwd),
             "gathered": {"gbs": gathered, "frac_of_hbm_peak": gathered / peak,
                          "bytes": st.nnz * cfg["d"] * es, "unique_rows": uniq, "lookups": st.nnz},
             "roofline": roofline,

@@ -222,6 +222,32 @@ int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d,
                          dlrm_stream_t stream);
 
 /*
+ * The two halves of dlrm_emb_bag_bwd_sgd, for callers that overlap them with
+ * other work.  dlrm_emb_bag_coalesce does the coalescing (the stable sort by
+ * (table, row) and the run-length encoding) into the workspace; it reads only
+ * rows, offsets and indices -- not the tables or the gradients -- so it can
+ * run on a second stream while the forward and interaction kernels run, or
+ * one step ahead.  dlrm_emb_bag_reduce_sgd then sums the pooled gradients of
+ * each run and applies the update, exactly as dlrm_emb_bag_bwd_sgd would.
+ *  - Both calls take the same T, d, nnz and B, and the same workspace
+ *    (dlrm_emb_bag_bwd_workspace_size bytes, 256-byte aligned); the reduce
+ *    must be given the rows the coalescing was given and be ordered after it
+ *    on the GPU (same stream, or an event).  None of this is checked.
+ *  - The workspace holds one coalescing at a time: a second coalesce into it
+ *    before the reduce has run replaces the first.
+ *  - The view (optional) is filled by the coalesce call, as in
+ *    dlrm_emb_bag_bwd_sgd.
+ */
+int dlrm_emb_bag_coalesce(const int64_t *rows, int T, int d, const int64_t *offsets, const int64_t *indices,
+                          int64_t nnz, int64_t B, void *workspace, size_t workspace_bytes,
+                          dlrm_coalesced_view *view, int32_t *err_flag, dlrm_stream_t stream);
+int dlrm_emb_bag_reduce_sgd(void *const *tables, const int64_t *rows, int T, int d, int dtype, int64_t nnz,
+                            int64_t B, const float *dpooled, int64_t dp_sample_stride,
+                            int64_t dp_table_stride, float lr, float *grad_rows, int64_t grad_rows_cap,
+                            void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                            dlrm_stream_t stream);
+
+/*
  * dlrm_emb_bag_bwd_sgd for callers that cannot allocate device memory (the
  * pages have no counterpart to this; it is a deployment aid).  Some callers
  * can neither call cudaMalloc nor hand the library a workspace -- a plugin

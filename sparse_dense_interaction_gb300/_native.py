@@ -50,6 +50,10 @@ SIGNATURES = {
                                             _vp, _vp]),
     "dlrm_emb_bag_interact_fwd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64, _i32,
                                          _vp, _i64, _vp, _i64, _i64, _vp, _vp]),
+    "dlrm_emb_bag_coalesce": (_i32, [_vp, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _sz,
+                                     ctypes.POINTER(CoalescedView), _vp, _vp]),
+    "dlrm_emb_bag_reduce_sgd": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _vp, _i64, _i64, _f32, _vp, _i64,
+                                       _vp, _sz, _vp, _vp]),
     "dlrm_read_error": (_i32, [_vp, _vp]),
     "dlrm_clear_error": (_i32, [_vp, _vp]),
     "dlrm_status_string": (ctypes.c_char_p, [_i32]),
@@ -182,8 +186,10 @@ def dlrm_emb_bag_bwd_sgd(tables, offsets, indices, B: int, dpooled, lr: float, w
                                        workspace.numel() * workspace.element_size(),
                                        ctypes.byref(view) if want_view else None, _ptr(err_flag),
                                        _stream(stream)), "dlrm_emb_bag_bwd_sgd")
-    if not want_view:
-        return None
+    return _view_tensors(view, workspace, nnz) if want_view else None
+
+
+def _view_tensors(view, workspace, nnz):
     base = workspace.data_ptr()
 
     def sub(ptr, n, dt):
@@ -196,6 +202,35 @@ def dlrm_emb_bag_bwd_sgd(tables, offsets, indices, B: int, dpooled, lr: float, w
                 uniq_row=sub(view.uniq_row, nnz, torch.int32),
                 seg_off=sub(view.seg_off, nnz + 1, torch.int32),
                 num_unique=sub(view.num_unique, 1, torch.int64))
+
+
+def dlrm_emb_bag_coalesce(rows, d: int, offsets, indices, B: int, workspace, err_flag=None, stream=None,
+                          want_view: bool = False):
+    """The coalescing half of :func:`dlrm_emb_bag_bwd_sgd` (reads only
+    ``rows``, a list of T table row counts, and the lookups)."""
+    T = len(rows)
+    r = (ctypes.c_int64 * max(T, 1))(*rows)
+    view = CoalescedView()
+    nnz = indices.numel()
+    _check(load().dlrm_emb_bag_coalesce(r, T, d, offsets.data_ptr(), _ptr(indices), nnz, B,
+                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                        ctypes.byref(view) if want_view else None, _ptr(err_flag),
+                                        _stream(stream)), "dlrm_emb_bag_coalesce")
+    return _view_tensors(view, workspace, nnz) if want_view else None
+
+
+def dlrm_emb_bag_reduce_sgd(tables, nnz: int, B: int, dpooled, lr: float, workspace, grad_rows=None,
+                            err_flag=None, stream=None):
+    """The reduce + update half of :func:`dlrm_emb_bag_bwd_sgd`, on a
+    workspace filled by :func:`dlrm_emb_bag_coalesce`."""
+    ptrs, rows, T, d, dtype = _tables(tables)
+    if dpooled.stride(2) != 1:
+        raise ValueError("dpooled must have unit stride in its last dimension")
+    cap = 0 if grad_rows is None else grad_rows.shape[0]
+    _check(load().dlrm_emb_bag_reduce_sgd(ptrs, rows, T, d, dtype, nnz, B, dpooled.data_ptr(), dpooled.stride(0),
+                                          dpooled.stride(1), float(lr), _ptr(grad_rows), cap,
+                                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                          _ptr(err_flag), _stream(stream)), "dlrm_emb_bag_reduce_sgd")
 
 
 def dlrm_emb_bag_interact_fwd(tables, offsets, indices, B: int, e0, include_self: bool, y, pooled=None,

@@ -54,6 +54,10 @@ size_t emb_bag_bwd_workspace(int, int64_t, int);
 int launch_emb_bag_bwd(const TableSet &, int, int, int, const int64_t *, const int64_t *, int64_t, int64_t,
                        const float *, int64_t, int64_t, float, float *, int64_t, void *, bool,
                        dlrm_coalesced_view *, int32_t *, cudaStream_t);
+int launch_coalesce(const TableSet &, int, int, const int64_t *, const int64_t *, int64_t, int64_t, void *,
+                    dlrm_coalesced_view *, int32_t *, cudaStream_t);
+int launch_reduce_sgd(const TableSet &, int, int, int, int64_t, int64_t, const float *, int64_t, int64_t, float,
+                      float *, int64_t, void *, bool, int32_t *, cudaStream_t);
 
 // Lookup positions are 32-bit in the backward's sort and scans; the bound
 // leaves headroom for tile and chunk arithmetic.
@@ -230,6 +234,42 @@ size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d)
     return emb_bag_bwd_workspace(T, nnz, d);
 }
 
+// Checks shared by the backward's calls: the sizes and the coalescing inputs.
+static int check_coalesce_args(int T, int d, const int64_t *offsets, const int64_t *indices, int64_t nnz,
+                               int64_t B, const void *workspace, size_t workspace_bytes)
+{
+    if (B < 0 || nnz < 0)
+        return DLRM_ERR_INVALID_ARG;
+    if (nnz > kMaxLookups || B > (int64_t)0x7fffffffLL)
+        return DLRM_ERR_UNSUPPORTED;
+    if (B == 0 && nnz != 0)  // no bags cannot hold lookups
+        return DLRM_ERR_INVALID_ARG;
+    if (!offsets || !workspace || !aligned(workspace, 256) || !aligned(offsets, 8))
+        return DLRM_ERR_INVALID_ARG;
+    if (nnz > 0 && (!indices || !aligned(indices, 8)))
+        return DLRM_ERR_INVALID_ARG;
+    if (workspace_bytes < emb_bag_bwd_workspace(T, nnz, d))
+        return DLRM_ERR_WORKSPACE_TOO_SMALL;
+    return DLRM_OK;
+}
+
+// Checks of the reduce's inputs: pooled gradients, learning rate, outputs.
+static int check_reduce_args(int64_t nnz, const float *dpooled, int64_t dp_sample_stride,
+                             int64_t dp_table_stride, float lr, const float *grad_rows, int64_t grad_rows_cap)
+{
+    if (dp_sample_stride < 0 || dp_table_stride < 0 || grad_rows_cap < 0)
+        return DLRM_ERR_INVALID_ARG;
+    if (dp_sample_stride > ((int64_t)1 << 29))  // the reduce addresses pooled rows with 32-bit byte strides
+        return DLRM_ERR_UNSUPPORTED;
+    if (!(lr == lr))  // NaN learning rate
+        return DLRM_ERR_INVALID_ARG;
+    if (nnz > 0 && (!dpooled || !aligned(dpooled, 4)))
+        return DLRM_ERR_INVALID_ARG;
+    if (grad_rows && !aligned(grad_rows, 4))
+        return DLRM_ERR_INVALID_ARG;
+    return DLRM_OK;
+}
+
 int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d, int dtype,
                          const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
                          const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride,
@@ -241,28 +281,65 @@ int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d,
     int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
     if (s != DLRM_OK)
         return s;
-    if (B < 0 || nnz < 0 || dp_sample_stride < 0 || dp_table_stride < 0 || grad_rows_cap < 0)
-        return DLRM_ERR_INVALID_ARG;
-    if (nnz > kMaxLookups || B > (int64_t)0x7fffffffLL)
-        return DLRM_ERR_UNSUPPORTED;
-    if (B == 0 && nnz != 0)  // no bags cannot hold lookups
-        return DLRM_ERR_INVALID_ARG;
-    if (dp_sample_stride > ((int64_t)1 << 29))  // the reduce addresses pooled rows with 32-bit byte strides
-        return DLRM_ERR_UNSUPPORTED;
-    if (!(lr == lr))  // NaN learning rate
-        return DLRM_ERR_INVALID_ARG;
-    if (!offsets || !workspace || !aligned(workspace, 256) || !aligned(offsets, 8))
-        return DLRM_ERR_INVALID_ARG;
-    if (nnz > 0 && (!indices || !aligned(indices, 8) || !dpooled || !aligned(dpooled, 4)))
-        return DLRM_ERR_INVALID_ARG;
-    if (grad_rows && !aligned(grad_rows, 4))
-        return DLRM_ERR_INVALID_ARG;
-    if (workspace_bytes < emb_bag_bwd_workspace(T, nnz, d))
-        return DLRM_ERR_WORKSPACE_TOO_SMALL;
+    if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=
+        DLRM_OK)
+        return s;
+    if ((s = check_coalesce_args(T, d, offsets, indices, nnz, B, workspace, workspace_bytes)) != DLRM_OK)
+        return s;
     const bool vec = emb_bag_bwd_vectorisable(ts, T, d, dpooled, dp_sample_stride, dp_table_stride, grad_rows);
     return launch_emb_bag_bwd(ts, T, d, dtype, offsets, indices, nnz, B, dpooled, dp_sample_stride,
                               dp_table_stride, lr, grad_rows, grad_rows ? grad_rows_cap : 0, workspace, vec,
                               view, err_flag, static_cast<cudaStream_t>(stream));
+}
+
+int dlrm_emb_bag_coalesce(const int64_t *rows, int T, int d, const int64_t *offsets, const int64_t *indices,
+                          int64_t nnz, int64_t B, void *workspace, size_t workspace_bytes,
+                          dlrm_coalesced_view *view, int32_t *err_flag, dlrm_stream_t stream)
+{
+    if (!rows || T <= 0 || d <= 0)
+        return DLRM_ERR_INVALID_ARG;
+    if (T > DLRM_MAX_TABLES)
+        return DLRM_ERR_UNSUPPORTED;
+    TableSet ts;
+    std::memset(&ts, 0, sizeof ts);
+    for (int t = 0; t < T; t++) {
+        if (rows[t] <= 0)
+            return DLRM_ERR_INVALID_ARG;
+        if (rows[t] > (int64_t)0xfffffffeLL)
+            return DLRM_ERR_UNSUPPORTED;
+        ts.rows[t] = rows[t];
+    }
+    int s = check_coalesce_args(T, d, offsets, indices, nnz, B, workspace, workspace_bytes);
+    if (s != DLRM_OK)
+        return s;
+    return launch_coalesce(ts, T, d, offsets, indices, nnz, B, workspace, view, err_flag,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int dlrm_emb_bag_reduce_sgd(void *const *tables, const int64_t *rows, int T, int d, int dtype, int64_t nnz,
+                            int64_t B, const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride,
+                            float lr, float *grad_rows, int64_t grad_rows_cap, void *workspace,
+                            size_t workspace_bytes, int32_t *err_flag, dlrm_stream_t stream)
+{
+    TableSet ts;
+    int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
+    if (s != DLRM_OK)
+        return s;
+    if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=
+        DLRM_OK)
+        return s;
+    if (B < 0 || nnz < 0 || (B == 0 && nnz != 0))
+        return DLRM_ERR_INVALID_ARG;
+    if (nnz > kMaxLookups || B > (int64_t)0x7fffffffLL)
+        return DLRM_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256))
+        return DLRM_ERR_INVALID_ARG;
+    if (workspace_bytes < emb_bag_bwd_workspace(T, nnz, d))
+        return DLRM_ERR_WORKSPACE_TOO_SMALL;
+    const bool vec = emb_bag_bwd_vectorisable(ts, T, d, dpooled, dp_sample_stride, dp_table_stride, grad_rows);
+    return launch_reduce_sgd(ts, T, d, dtype, nnz, B, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows,
+                             grad_rows ? grad_rows_cap : 0, workspace, vec, err_flag,
+                             static_cast<cudaStream_t>(stream));
 }
 
 int dlrm_read_error(const int32_t *err_flag, dlrm_stream_t stream)

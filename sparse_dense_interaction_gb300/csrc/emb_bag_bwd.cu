@@ -578,11 +578,8 @@ bool emb_bag_bwd_vectorisable(const TableSet &ts, int T, int d, const float *dpo
 
 size_t emb_bag_bwd_workspace(int T, int64_t nnz, int d) { return bwd_layout(T, nnz, d).total; }
 
-int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_t *offsets,
-                       const int64_t *indices, int64_t nnz, int64_t B, const float *dpooled,
-                       int64_t dpss, int64_t dpts, float lr, float *grad_rows, int64_t grad_cap,
-                       void *workspace, bool vec, dlrm_coalesced_view *view, int32_t *err,
-                       cudaStream_t st)
+// Device pointers of the workspace's regions.
+static BwdPtrs bind_workspace(int T, int64_t nnz, int d, void *workspace)
 {
     const BwdLayout L = bwd_layout(T, nnz, d);
     char *base = static_cast<char *>(workspace);
@@ -613,9 +610,26 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
     w.num_unique = reinterpret_cast<int64_t *>(base + L.num_unique);
     w.ntiles_max = L.ntiles_max;
 
-    const int bits = row_bits(ts, T);
-    const int passes = (bits + kRadixBits - 1) / kRadixBits;
-    const int final_buf = (passes - 1) & 1;
+    return w;
+}
+
+// Passes of the radix sort for these tables and the buffer that ends up
+// holding the sorted keys (both halves of the backward derive them alike).
+static void sort_plan(const TableSet &ts, int T, int &bits, int &passes, int &final_buf)
+{
+    bits = row_bits(ts, T);
+    passes = (bits + kRadixBits - 1) / kRadixBits;
+    final_buf = (passes - 1) & 1;
+}
+
+int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, const int64_t *indices,
+                    int64_t nnz, int64_t B, void *workspace, dlrm_coalesced_view *view, int32_t *err,
+                    cudaStream_t st)
+{
+    const BwdLayout L = bwd_layout(T, nnz, d);
+    BwdPtrs w = bind_workspace(T, nnz, d, workspace);
+    int bits, passes, final_buf;
+    sort_plan(ts, T, bits, passes, final_buf);
     if (view) {
         view->sorted_pos = w.vals[final_buf];
         view->sorted_row = w.keys[final_buf];
@@ -667,9 +681,19 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
         return s;
     seg_scan_kernel<<<1, 1024, 0, st>>>(T, nnz, w);
     count_launch(st);
-    if ((s = launch_status()) != DLRM_OK)
-        return s;
+    return launch_status();
+}
 
+int launch_reduce_sgd(const TableSet &ts, int T, int d, int dtype, int64_t nnz, int64_t B, const float *dpooled,
+                      int64_t dpss, int64_t dpts, float lr, float *grad_rows, int64_t grad_cap, void *workspace,
+                      bool vec, int32_t *err, cudaStream_t st)
+{
+    if (nnz == 0)
+        return DLRM_OK;
+    const BwdLayout L = bwd_layout(T, nnz, d);
+    BwdPtrs w = bind_workspace(T, nnz, d, workspace);
+    int bits, passes, final_buf;
+    sort_plan(ts, T, bits, passes, final_buf);
     ReduceArgs a;
     a.tables = ts;
     a.T = T;
@@ -683,7 +707,20 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
     a.grad_cap = grad_cap;
     a.final_buf = final_buf;
     a.err = err;
-    return launch_seg_reduce(dtype, a, w, grid, vec, st);
+    return launch_seg_reduce(dtype, a, w, L.ntiles_max, vec, st);
+}
+
+int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_t *offsets,
+                       const int64_t *indices, int64_t nnz, int64_t B, const float *dpooled,
+                       int64_t dpss, int64_t dpts, float lr, float *grad_rows, int64_t grad_cap,
+                       void *workspace, bool vec, dlrm_coalesced_view *view, int32_t *err,
+                       cudaStream_t st)
+{
+    const int s = launch_coalesce(ts, T, d, offsets, indices, nnz, B, workspace, view, err, st);
+    if (s != DLRM_OK)
+        return s;
+    return launch_reduce_sgd(ts, T, d, dtype, nnz, B, dpooled, dpss, dpts, lr, grad_rows, grad_cap, workspace,
+                             vec, err, st);
 }
 
 }  // namespace dlrm
