@@ -74,8 +74,10 @@ def _load():
             lib.oracle_coalesce.argtypes = [i32, i64, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp]
             lib.oracle_sgd.argtypes = [i32, i32, i32, vp, vp, i64, vp, i64, dp, dp,
                                        ctypes.c_double, vp, vp, vp, vp, i64, dp, dp, dp, dp]
+            lib.oracle_adagrad.argtypes = [i32, i32, i32, vp, vp, i64, vp, i64, dp, dp, ctypes.c_double,
+                                           ctypes.c_double, vp, vp, vp, vp, i64, dp, dp, dp, dp, dp, dp, dp]
             for name in ("oracle_decode", "oracle_emb_bag_fwd", "oracle_interact_fwd",
-                         "oracle_interact_bwd", "oracle_coalesce", "oracle_sgd"):
+                         "oracle_interact_bwd", "oracle_coalesce", "oracle_sgd", "oracle_adagrad"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -189,6 +191,37 @@ def coalesce(rows, offsets, indices, B: int):
     u = int(U[0])
     return dict(sorted_pos=sorted_pos, sorted_row=sorted_row, uniq_table=uniq_table[:u].copy(),
                 uniq_row=uniq_row[:u].copy(), seg_off=seg_off[:u + 1].copy(), U=u)
+
+
+def adagrad(tables, dtype: str, offsets, B: int, nnz: int, dpooled, lr: float, eps: float, state, co: dict,
+            dpooled_mag=None):
+    """Row-wise AdaGrad on the coalesced gradients, one result per unique key.
+
+    ``state`` holds the accumulator of each unique key of ``co`` (the result of
+    :func:`coalesce`), in that order.  Returns (grad, grad_mag, new_state,
+    new_state_mag, new_row, new_row_mag) in fp64: [U][d], [U], [U][d].
+    """
+    held, arr, rows = _tables_arg(tables, dtype)
+    T, d = len(held), held[0].shape[1]
+    offsets = _i64(offsets)
+    dpooled = _f64(dpooled)
+    U = co["U"]
+    grad = np.empty((U, d), dtype=np.float64)
+    gm = np.empty_like(grad)
+    ns = np.empty(U, dtype=np.float64)
+    nsm = np.empty_like(ns)
+    nr = np.empty_like(grad)
+    nrm = np.empty_like(grad)
+    sp = _i64(co["sorted_pos"])
+    ut = np.ascontiguousarray(co["uniq_table"], dtype=np.int32)
+    ur = _i64(co["uniq_row"])
+    so = _i64(co["seg_off"])
+    st = _f64(np.asarray(state, dtype=np.float64).reshape(U))
+    _check(_load().oracle_adagrad(T, d, _DTYPE_CODES[dtype], arr, _ptr(rows), B, _ptr(offsets), nnz,
+                                  _ptr(dpooled), _ptr(_f64(dpooled_mag)), float(lr), float(eps), _ptr(sp),
+                                  _ptr(ut), _ptr(ur), _ptr(so), U, _ptr(st), _ptr(grad), _ptr(gm), _ptr(ns),
+                                  _ptr(nsm), _ptr(nr), _ptr(nrm)), "adagrad")
+    return grad, gm, ns, nsm, nr, nrm
 
 
 def sgd(tables, dtype: str, offsets, B: int, nnz: int, dpooled, lr: float, co: dict,

@@ -403,3 +403,72 @@ int oracle_sgd(int T, int d, int dtype, const void *const *tables, const int64_t
     free(bag_of);
     return ORACLE_OK;
 }
+
+/*
+ * Row-wise AdaGrad on the coalesced gradient.  The notes name AdaGrad as the
+ * usual optimizer ("Notes/DLRM", section 5, Training) without its formula;
+ * this is AdaGrad (Duchi, Hazan and Singer, 2011) with one accumulator per
+ * row: the accumulator grows by the mean over the row of the squared
+ * gradient, and every element of the row takes the same step size.
+ *
+ *   g[u]       = sum over the lookups of key u of dpooled    (as in oracle_sgd)
+ *   s'         = s + (1/d) sum_e g[u][e]^2
+ *   w'[e]      = w[e] - lr * g[u][e] / (sqrt(s') + eps)
+ *
+ * state[u] is s for key u (in), new_state[u] is s'.  Magnitudes bound the
+ * effect of any summation order to first order, so that a result may differ
+ * from the fp64 value by at most rel * magnitude:
+ *   grad_mag   sum of |terms| (as in oracle_sgd);
+ *   state_mag  s + (1/d) sum_e (2 |g| grad_mag + g^2): a change of g by
+ *              rel * grad_mag moves g^2 by 2 |g| rel * grad_mag; g^2 covers
+ *              the rounding of the squares and of their sum;
+ *   row_mag    |w| + k (grad_mag + |g|) + |g| lr state_mag / (2 sqrt(s') r^2)
+ *              with r = sqrt(s') + eps and k = lr / r: the first terms cover
+ *              the change of g and the rounding of k g, the last the change
+ *              of k when s' moves by rel * state_mag.
+ * A row whose gradient is zero everywhere keeps w (its step is 0 / r).
+ */
+int oracle_adagrad(int T, int d, int dtype, const void *const *tables, const int64_t *rows,
+                   int64_t B, const int64_t *offsets, int64_t nnz,
+                   const double *dpooled, const double *dpooled_mag, double lr, double eps,
+                   const int64_t *sorted_pos, const int32_t *uniq_table, const int64_t *uniq_row,
+                   const int64_t *seg_off, int64_t U, const double *state,
+                   double *grad, double *grad_mag, double *new_state, double *new_state_mag,
+                   double *new_row, double *new_row_mag)
+{
+    if (T <= 0 || d <= 0 || B < 0 || nnz < 0 || U < 0 || !(eps >= 0.0))
+        return ORACLE_INVALID_ARG;
+    /* the gradients, exactly as the SGD oracle sums them */
+    int st = oracle_sgd(T, d, dtype, tables, rows, B, offsets, nnz, dpooled, dpooled_mag, 0.0, sorted_pos,
+                        uniq_table, uniq_row, seg_off, U, grad, grad_mag, new_row, new_row_mag);
+    if (st != ORACLE_OK)
+        return st;
+    for (int64_t u = 0; u < U; u++) {
+        const int t = uniq_table[u];
+        const int64_t r = uniq_row[u];
+        const double *g = grad + u * d, *gm = grad_mag + u * d;
+        double q = 0.0, qm = 0.0;
+        for (int e = 0; e < d; e++) {
+            q += g[e] * g[e];
+            qm += 2.0 * fabs(g[e]) * gm[e] + g[e] * g[e];
+        }
+        const double s1 = state[u] + q / d;
+        new_state[u] = s1;
+        new_state_mag[u] = fabs(state[u]) + qm / d;
+        const double root = sqrt(s1), den = root + eps;
+        for (int e = 0; e < d; e++) {
+            const double w = table_element(tables[t], dtype, r * d + e);
+            if (g[e] == 0.0) {
+                new_row[u * d + e] = w;
+                new_row_mag[u * d + e] = fabs(w) + (den > 0.0 ? fabs(lr) / den * gm[e] : 0.0);
+                continue;
+            }
+            const double k = lr / den;
+            new_row[u * d + e] = w - k * g[e];
+            new_row_mag[u * d + e] = fabs(w) + fabs(k) * (gm[e] + fabs(g[e])) +
+                                     fabs(g[e]) * fabs(lr) * new_state_mag[u] / (2.0 * root * den * den);
+        }
+    }
+    return ORACLE_OK;
+}
+

@@ -395,3 +395,83 @@ def test_sgd_reads_half_tables_exactly(dtype):
         wrow = (_bf16_bits_to_f64(tables[t][r]) if dtype == "bf16"
                 else tables[t][r].astype(np.float64))
         np.testing.assert_allclose(new_row[u], wrow - 0.01 * grad[u], rtol=0, atol=1e-15)
+
+
+# ------------------------------------------------------- row-wise AdaGrad ---
+
+def _worked_tables(g):
+    return [g["table0"].reshape(3, 2).astype(np.float32), g["table1"].reshape(2, 2).astype(np.float32)]
+
+
+def test_adagrad_worked_example():
+    g = _golden.load("emb_bag_worked_example.txt")
+    a = _golden.load("adagrad_worked_example.txt")
+    co = oracle.coalesce([3, 2], g["offsets"], g["indices"], 2)
+    _, _, ns, _, nr, _ = oracle.adagrad(_worked_tables(g), "f32", g["offsets"], 2, 6, g["dpooled"].reshape(2, 2, 2),
+                                        float(a["lr"][0]), float(a["eps"][0]), a["state"], co)
+    np.testing.assert_array_equal(ns, a["new_state"])
+    np.testing.assert_allclose(nr.reshape(-1), a["new_row"], rtol=1e-15, atol=0)
+
+
+def _one_lookup(c, d=8, w=None):
+    """One table, one bag holding one lookup of row 2, pooled gradient c everywhere."""
+    tables = [np.zeros((4, d), dtype=np.float32) if w is None else w]
+    offsets, indices = np.array([0, 1]), np.array([2])
+    co = oracle.coalesce([4], offsets, indices, 1)
+    return tables, offsets, co, np.full((1, 1, d), c)
+
+
+def test_adagrad_constant_gradient_closed_form():
+    # from s = 0 with eps = 0 a constant gradient c moves every element by lr * sign(c);
+    # the second step sees s = c^2 and moves it by lr * sign(c) / sqrt(2)
+    lr, c = 0.25, -0.75
+    tables, offsets, co, dp = _one_lookup(c)
+    _, _, s1, _, w1, _ = oracle.adagrad(tables, "f32", offsets, 1, 1, dp, lr, 0.0, [0.0], co)
+    assert s1[0] == c * c
+    np.testing.assert_array_equal(w1[0], np.full(8, lr))
+    tables[0][2] = w1[0].astype(np.float32)
+    _, _, s2, _, w2, _ = oracle.adagrad(tables, "f32", offsets, 1, 1, dp, lr, 0.0, s1, co)
+    assert s2[0] == 2 * c * c
+    np.testing.assert_allclose(w2[0], lr + lr / np.sqrt(2.0), rtol=1e-15)
+
+
+def test_adagrad_first_step_is_scale_invariant():
+    # s' = mean g^2 from s = 0: scaling every gradient leaves the step unchanged
+    rng = np.random.default_rng(4)
+    rows, T, B, d = [9, 5], 2, 6, 4
+    tables = [rng.standard_normal((r, d)).astype(np.float32) for r in rows]
+    offsets, indices = _csr(_random_bags(rng, T, B, rows, 4))
+    dp = rng.standard_normal((B, T, d))
+    co = oracle.coalesce(rows, offsets, indices, B)
+    z = np.zeros(co["U"])
+    r1 = oracle.adagrad(tables, "f32", offsets, B, indices.size, dp, 0.1, 0.0, z, co)[4]
+    r2 = oracle.adagrad(tables, "f32", offsets, B, indices.size, dp * 1024.0, 0.1, 0.0, z, co)[4]
+    np.testing.assert_allclose(r1, r2, rtol=1e-13, atol=1e-13)
+
+
+def test_adagrad_with_a_huge_accumulator_is_sgd_with_a_scaled_rate():
+    # s = 1e24: sqrt(s') = 1e12 up to a relative 1e-20, so the step is SGD at lr / 1e12
+    rng = np.random.default_rng(6)
+    rows, T, B, d = [7, 8, 3], 3, 10, 3
+    tables = [rng.standard_normal((r, d)).astype(np.float32) for r in rows]
+    offsets, indices = _csr(_random_bags(rng, T, B, rows, 5))
+    dp = rng.standard_normal((B, T, d))
+    co = oracle.coalesce(rows, offsets, indices, B)
+    lr = 3e11
+    g, _, _, _, nr, _ = oracle.adagrad(tables, "f32", offsets, B, indices.size, dp, lr, 0.0, np.full(co["U"], 1e24), co)
+    g2, _, sgd_row, _ = oracle.sgd(tables, "f32", offsets, B, indices.size, dp, lr / 1e12, co)
+    np.testing.assert_array_equal(g, g2)
+    np.testing.assert_allclose(nr, sgd_row, rtol=1e-14, atol=1e-14)
+
+
+def test_adagrad_zero_rate_and_zero_gradient():
+    # lr = 0 keeps the row and still grows the accumulator; a zero gradient keeps both
+    w = np.arange(32, dtype=np.float32).reshape(4, 8)
+    tables, offsets, co, dp = _one_lookup(0.5, w=w)
+    _, _, s, _, nr, _ = oracle.adagrad(tables, "f32", offsets, 1, 1, dp, 0.0, 1e-8, [2.0], co)
+    assert s[0] == 2.0 + 0.25
+    np.testing.assert_array_equal(nr[0], w[2])
+    tables, offsets, co, dp = _one_lookup(0.0, w=w)
+    _, _, s, _, nr, _ = oracle.adagrad(tables, "f32", offsets, 1, 1, dp, 0.1, 1e-8, [2.0], co)
+    assert s[0] == 2.0
+    np.testing.assert_array_equal(nr[0], w[2])
