@@ -59,6 +59,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--schedule", choices=["overlap", "serial"], default="overlap",
                    help="overlap: the backward's coalescing runs on a side stream next to the forward")
+    p.add_argument("--optimizer", choices=["sgd", "adagrad"], default="sgd",
+                   help="row-wise update of the touched rows (adagrad: one fp32 accumulator per row)")
     p.add_argument("--fwd", choices=["separate", "fused"], default="separate",
                    help="fused: one kernel for the lookup and the interaction forward")
     p.add_argument("--batch", type=int, default=None, help="override the batch size (profiling runs)")
@@ -116,7 +118,7 @@ def oracle_sample(cfg, offsets, indices, Bs, seed):
                 dpooled=W.make_dpooled(cfg, seed)[:Bs])
 
 
-def oracle_step(s):
+def oracle_step(s, optimizer="sgd"):
     import oracle
     cfg = s["cfg"]
     B, dt = cfg["B"], cfg["dtype"]
@@ -127,27 +129,31 @@ def oracle_step(s):
     else:
         dp, dpm = s["dpooled"], None
     co = oracle.coalesce(cfg["rows"], s["offsets"], s["indices"], B)
-    oracle.sgd(s["tables"], dt, s["offsets"], B, s["indices"].size, dp, cfg["lr"], co, dpooled_mag=dpm)
+    if optimizer == "adagrad":
+        oracle.adagrad(s["tables"], dt, s["offsets"], B, s["indices"].size, dp, cfg["lr"], ADAGRAD_EPS,
+                       np.zeros(co["U"]), co, dpooled_mag=dpm)
+    else:
+        oracle.sgd(s["tables"], dt, s["offsets"], B, s["indices"].size, dp, cfg["lr"], co, dpooled_mag=dpm)
 
 
-def calibrate_oracle(cfg, offsets, indices, seed, seconds):
+def calibrate_oracle(cfg, offsets, indices, seed, seconds, optimizer="sgd"):
     """Picks a sample size whose oracle step takes about `seconds`."""
     probe = min(128, cfg["B"])
     s = oracle_sample(cfg, offsets, indices, probe, seed)
-    oracle_step(s)  # first call loads the library and warms the caches
+    oracle_step(s, optimizer)  # first call loads the library and warms the caches
     t0 = time.perf_counter()
-    oracle_step(s)
+    oracle_step(s, optimizer)
     per_sample = (time.perf_counter() - t0) / probe
     return int(max(probe, min(cfg["B"], seconds / max(per_sample, 1e-9))))
 
 
-def cpu_baseline(cfg, offsets, indices, seed, seconds):
+def cpu_baseline(cfg, offsets, indices, seed, seconds, optimizer="sgd"):
     import oracle
     oracle.build()
-    Bs = calibrate_oracle(cfg, offsets, indices, seed, seconds)
+    Bs = calibrate_oracle(cfg, offsets, indices, seed, seconds, optimizer)
     s = oracle_sample(cfg, offsets, indices, Bs, seed)
     t0 = time.perf_counter()
-    oracle_step(s)
+    oracle_step(s, optimizer)
     el = time.perf_counter() - t0
     return {"value": Bs / el, "unit": "samples/s", "cores": 1, "kind": "oracle",
             "sample": f"first {Bs} of {cfg['B']} samples of the same batch (all {cfg['T']} tables, "
@@ -163,13 +169,13 @@ def run_reference(args):
     cfg = workload_config(args)
     offsets, indices = W.make_indices(cfg, args.seed)
     budget = 90.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
-    Bs = calibrate_oracle(cfg, offsets, indices, args.seed, min(3.0, budget))
+    Bs = calibrate_oracle(cfg, offsets, indices, args.seed, min(3.0, budget), args.optimizer)
     s = oracle_sample(cfg, offsets, indices, Bs, args.seed)
     for _ in range(args.warmup):
-        oracle_step(s)
+        oracle_step(s, args.optimizer)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(s)
+        oracle_step(s, args.optimizer)
     el = time.perf_counter() - t0
     value = Bs * args.steps / el
     sample = (f"first {Bs} of {cfg['B']} samples of the batch per step (all {cfg['T']} tables, "
@@ -179,7 +185,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(config_of(cfg), schedule=args.schedule, forward=args.fwd),
+        "config": dict(config_of(cfg), schedule=args.schedule, forward=args.fwd, optimizer=args.optimizer),
         "cpu_baseline": {"value": value, "unit": "samples/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -263,10 +269,13 @@ class ClockSampler:
 
 # ------------------------------------------------------------ the GPU run ---
 
+ADAGRAD_EPS = 1e-8
+
+
 class Step:
     """Device buffers and the launches of one step of the path."""
 
-    def __init__(self, cfg, seed, dev, schedule="overlap", fwd="separate"):
+    def __init__(self, cfg, seed, dev, schedule="overlap", fwd="separate", optimizer="sgd"):
         import torch
 
         import sparse_dense_interaction_gb300 as sdi
@@ -292,7 +301,9 @@ class Step:
                               device=dev)
         self.grad = torch.empty((self.nnz, d), device=dev) if cfg["update"] == "grad" else None
         self.flag = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.schedule, self.fwd = schedule, fwd
+        self.schedule, self.fwd, self.optimizer = schedule, fwd, optimizer
+        self.state = ([torch.zeros(r, dtype=torch.float32, device=dev) for r in cfg["rows"]]
+                      if optimizer == "adagrad" else None)
         self.side = torch.cuda.Stream(dev)
         self.coalesced = torch.cuda.Event()
 
@@ -334,13 +345,22 @@ class Step:
                 self.e0, self.pooled, c["include_self"], self.dy, self.de0, self.dpooled), main)
         if self.schedule == "overlap":
             main.wait_event(self.coalesced)
-            call("reduce_sgd", lambda: sdi.dlrm_emb_bag_reduce_sgd(
-                self.tables, self.nnz, c["B"], self.dpooled, c["lr"], self.ws, grad_rows=self.grad,
-                err_flag=self.flag), main)
-        else:
+            if self.state is None:
+                call("reduce_sgd", lambda: sdi.dlrm_emb_bag_reduce_sgd(
+                    self.tables, self.nnz, c["B"], self.dpooled, c["lr"], self.ws, grad_rows=self.grad,
+                    err_flag=self.flag), main)
+            else:
+                call("reduce_sgd", lambda: sdi.dlrm_emb_bag_reduce_adagrad(
+                    self.tables, self.state, self.nnz, c["B"], self.dpooled, c["lr"], ADAGRAD_EPS, self.ws,
+                    grad_rows=self.grad, err_flag=self.flag), main)
+        elif self.state is None:
             call("emb_bag_bwd", lambda: sdi.dlrm_emb_bag_bwd_sgd(
                 self.tables, self.offsets, self.indices, c["B"], self.dpooled, c["lr"], self.ws,
                 grad_rows=self.grad, err_flag=self.flag), main)
+        else:
+            call("emb_bag_bwd", lambda: sdi.dlrm_emb_bag_bwd_adagrad(
+                self.tables, self.state, self.offsets, self.indices, c["B"], self.dpooled, c["lr"], ADAGRAD_EPS,
+                self.ws, grad_rows=self.grad, err_flag=self.flag), main)
 
 
 class KernelProfiler:
@@ -435,6 +455,8 @@ def algorithmic_bytes(cfg, st):
     # the reduce + update kernel: sorted keys and positions, bag ids, the
     # pooled gradient, and one read-modify-write of every unique row
     out["seg_reduce"] = st.nnz * 12 + nb * d * 4 + 2 * uniq * d * es
+    if st.state is not None:  # AdaGrad: read-modify-write of each touched row's accumulator
+        out["seg_reduce"] += 2 * uniq * 4
     return out, uniq
 
 
@@ -459,7 +481,7 @@ def run_ours(args):
     sdi.load()
 
     cfg = workload_config(args)
-    st = Step(cfg, args.seed + rank, dev, args.schedule, args.fwd)
+    st = Step(cfg, args.seed + rank, dev, args.schedule, args.fwd, args.optimizer)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         st.run()
@@ -527,14 +549,14 @@ def run_ours(args):
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(cfg, st.offsets_h, st.indices_h, args.seed, args.cpu_seconds)
+        base = cpu_baseline(cfg, st.offsets_h, st.indices_h, args.seed, args.cpu_seconds, args.optimizer)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 accumulate, " + cfg["dtype"] + " tables",
             "data": "synthetic (seeded; Zipf/uniform indices, counter-hash tables)",
-            "config": dict(config_of(cfg), schedule=args.schedule, forward=args.fwd),
+            "config": dict(config_of(cfg), schedule=args.schedule, forward=args.fwd, optimizer=args.optimizer),
             "gathered": {"gbs": gathered, "frac_of_hbm_peak": gathered / peak,
                          "bytes": st.nnz * cfg["d"] * es, "unique_rows": uniq, "lookups": st.nnz},
             "roofline": roofline,

@@ -248,6 +248,39 @@ int dlrm_emb_bag_reduce_sgd(void *const *tables, const int64_t *rows, int T, int
                             dlrm_stream_t stream);
 
 /*
+ * Embedding-bag backward with row-wise AdaGrad ("Notes/DLRM", section 5: the
+ * optimizer is typically adaptive, Adam or AdaGrad; the notes give no
+ * formula, and this is AdaGrad with one accumulator per row).  The coalescing
+ * and the coalesced gradient g_u are those of dlrm_emb_bag_bwd_sgd; then, for
+ * every unique key u = (t, r), in fp32:
+ *
+ *   state[t][r] <- s' = state[t][r] + (1/d) sum_e g_u[e]^2
+ *   tables[t][r][e] <- tables[t][r][e] - lr * g_u[e] / (sqrt(s') + eps)
+ *                      (one fused multiply-add, one rounding to the table type)
+ *
+ * state   host array of T device pointers, each fp32 [rows[t]], 4-byte
+ *         aligned: the accumulators, updated in place for touched rows only
+ *         (start them at 0 for plain AdaGrad).
+ * eps     > 0 and finite (it keeps the step of an all-zero gradient at 0).
+ * lr == 0 leaves tables and accumulators untouched.  d may be at most 256
+ * (DLRM_ERR_UNSUPPORTED beyond): the update needs a row's whole gradient in
+ * registers.  The other arguments are those of dlrm_emb_bag_bwd_sgd;
+ * dlrm_emb_bag_reduce_adagrad is the reduce half, used after
+ * dlrm_emb_bag_coalesce exactly as dlrm_emb_bag_reduce_sgd is.
+ */
+int dlrm_emb_bag_bwd_adagrad(void *const *tables, float *const *state, const int64_t *rows, int T, int d,
+                             int dtype, const int64_t *offsets, const int64_t *indices, int64_t nnz,
+                             int64_t B, const float *dpooled, int64_t dp_sample_stride,
+                             int64_t dp_table_stride, float lr, float eps, float *grad_rows,
+                             int64_t grad_rows_cap, void *workspace, size_t workspace_bytes,
+                             dlrm_coalesced_view *view, int32_t *err_flag, dlrm_stream_t stream);
+int dlrm_emb_bag_reduce_adagrad(void *const *tables, float *const *state, const int64_t *rows, int T, int d,
+                                int dtype, int64_t nnz, int64_t B, const float *dpooled,
+                                int64_t dp_sample_stride, int64_t dp_table_stride, float lr, float eps,
+                                float *grad_rows, int64_t grad_rows_cap, void *workspace,
+                                size_t workspace_bytes, int32_t *err_flag, dlrm_stream_t stream);
+
+/*
  * dlrm_emb_bag_bwd_sgd for callers that cannot allocate device memory (the
  * pages have no counterpart to this; it is a deployment aid).  Some callers
  * can neither call cudaMalloc nor hand the library a workspace -- a plugin

@@ -54,6 +54,11 @@ SIGNATURES = {
                                      ctypes.POINTER(CoalescedView), _vp, _vp]),
     "dlrm_emb_bag_reduce_sgd": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i64, _vp, _i64, _i64, _f32, _vp, _i64,
                                        _vp, _sz, _vp, _vp]),
+    "dlrm_emb_bag_bwd_adagrad": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64, _i64,
+                                        _f32, _f32, _vp, _i64, _vp, _sz, ctypes.POINTER(CoalescedView), _vp,
+                                        _vp]),
+    "dlrm_emb_bag_reduce_adagrad": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i64, _i64, _vp, _i64, _i64, _f32,
+                                           _f32, _vp, _i64, _vp, _sz, _vp, _vp]),
     "dlrm_read_error": (_i32, [_vp, _vp]),
     "dlrm_clear_error": (_i32, [_vp, _vp]),
     "dlrm_status_string": (ctypes.c_char_p, [_i32]),
@@ -252,6 +257,50 @@ def dlrm_emb_bag_interact_fwd(tables, offsets, indices, B: int, e0, include_self
                                             1 if include_self else 0, y.data_ptr(), y.stride(0), _ptr(pooled),
                                             pss, pts, _ptr(err_flag), _stream(stream)),
            "dlrm_emb_bag_interact_fwd")
+
+
+def _states(state, tables):
+    if len(state) != len(tables):
+        raise ValueError("one accumulator array per table")
+    for s, t in zip(state, tables):
+        if s.dtype != torch.float32 or s.dim() != 1 or s.shape[0] != t.shape[0] or s.stride(0) != 1:
+            raise ValueError("each accumulator array is a contiguous fp32 [rows] tensor")
+    return (ctypes.c_void_p * max(len(state), 1))(*[s.data_ptr() for s in state])
+
+
+def dlrm_emb_bag_bwd_adagrad(tables, state, offsets, indices, B: int, dpooled, lr: float, eps: float, workspace,
+                             grad_rows=None, err_flag=None, stream=None, want_view: bool = False):
+    """:func:`dlrm_emb_bag_bwd_sgd` with row-wise AdaGrad: ``state`` is a list
+    of fp32 [rows] accumulators, one per table, updated in place."""
+    ptrs, rows, T, d, dtype = _tables(tables)
+    st = _states(state, tables)
+    if dpooled.stride(2) != 1:
+        raise ValueError("dpooled must have unit stride in its last dimension")
+    view = CoalescedView()
+    nnz = indices.numel()
+    cap = 0 if grad_rows is None else grad_rows.shape[0]
+    _check(load().dlrm_emb_bag_bwd_adagrad(ptrs, st, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices), nnz, B,
+                                           dpooled.data_ptr(), dpooled.stride(0), dpooled.stride(1), float(lr),
+                                           float(eps), _ptr(grad_rows), cap, workspace.data_ptr(),
+                                           workspace.numel() * workspace.element_size(),
+                                           ctypes.byref(view) if want_view else None, _ptr(err_flag),
+                                           _stream(stream)), "dlrm_emb_bag_bwd_adagrad")
+    return _view_tensors(view, workspace, nnz) if want_view else None
+
+
+def dlrm_emb_bag_reduce_adagrad(tables, state, nnz: int, B: int, dpooled, lr: float, eps: float, workspace,
+                                grad_rows=None, err_flag=None, stream=None):
+    """The reduce + AdaGrad half, on a workspace filled by :func:`dlrm_emb_bag_coalesce`."""
+    ptrs, rows, T, d, dtype = _tables(tables)
+    st = _states(state, tables)
+    if dpooled.stride(2) != 1:
+        raise ValueError("dpooled must have unit stride in its last dimension")
+    cap = 0 if grad_rows is None else grad_rows.shape[0]
+    _check(load().dlrm_emb_bag_reduce_adagrad(ptrs, st, rows, T, d, dtype, nnz, B, dpooled.data_ptr(),
+                                              dpooled.stride(0), dpooled.stride(1), float(lr), float(eps),
+                                              _ptr(grad_rows), cap, workspace.data_ptr(),
+                                              workspace.numel() * workspace.element_size(), _ptr(err_flag),
+                                              _stream(stream)), "dlrm_emb_bag_reduce_adagrad")
 
 
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024

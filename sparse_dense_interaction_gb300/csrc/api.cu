@@ -57,7 +57,7 @@ int launch_emb_bag_bwd(const TableSet &, int, int, int, const int64_t *, const i
 int launch_coalesce(const TableSet &, int, int, const int64_t *, const int64_t *, int64_t, int64_t, void *,
                     dlrm_coalesced_view *, int32_t *, cudaStream_t);
 int launch_reduce_sgd(const TableSet &, int, int, int, int64_t, int64_t, const float *, int64_t, int64_t, float,
-                      float *, int64_t, void *, bool, int32_t *, cudaStream_t);
+                      float *, int64_t, void *, bool, int32_t *, cudaStream_t, float, float *const *);
 
 // Lookup positions are 32-bit in the backward's sort and scans; the bound
 // leaves headroom for tile and chunk arithmetic.
@@ -339,7 +339,76 @@ int dlrm_emb_bag_reduce_sgd(void *const *tables, const int64_t *rows, int T, int
     const bool vec = emb_bag_bwd_vectorisable(ts, T, d, dpooled, dp_sample_stride, dp_table_stride, grad_rows);
     return launch_reduce_sgd(ts, T, d, dtype, nnz, B, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows,
                              grad_rows ? grad_rows_cap : 0, workspace, vec, err_flag,
-                             static_cast<cudaStream_t>(stream));
+                             static_cast<cudaStream_t>(stream), 0.f, nullptr);
+}
+
+// Checks of the AdaGrad arguments: one fp32 accumulator array per table,
+// a positive finite eps, rows short enough to be held whole.
+static int check_adagrad(float *const *state, int T, int d, float lr, float eps)
+{
+    if (!state || !(eps > 0.f) || !(eps <= 3.0e38f) || !(lr == lr) || lr > 3.0e38f || lr < -3.0e38f)
+        return DLRM_ERR_INVALID_ARG;
+    for (int t = 0; t < T; t++)
+        if (!state[t] || !aligned(state[t], 4))
+            return DLRM_ERR_INVALID_ARG;
+    if (d > 256)
+        return DLRM_ERR_UNSUPPORTED;
+    return DLRM_OK;
+}
+
+int dlrm_emb_bag_bwd_adagrad(void *const *tables, float *const *state, const int64_t *rows, int T, int d, int dtype,
+                             const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                             const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride, float lr,
+                             float eps, float *grad_rows, int64_t grad_rows_cap, void *workspace,
+                             size_t workspace_bytes, dlrm_coalesced_view *view, int32_t *err_flag,
+                             dlrm_stream_t stream)
+{
+    TableSet ts;
+    int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
+    if (s != DLRM_OK)
+        return s;
+    if ((s = check_adagrad(state, T, d, lr, eps)) != DLRM_OK)
+        return s;
+    if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=
+        DLRM_OK)
+        return s;
+    if ((s = check_coalesce_args(T, d, offsets, indices, nnz, B, workspace, workspace_bytes)) != DLRM_OK)
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((s = launch_coalesce(ts, T, d, offsets, indices, nnz, B, workspace, view, err_flag, st)) != DLRM_OK)
+        return s;
+    const bool vec = emb_bag_bwd_vectorisable(ts, T, d, dpooled, dp_sample_stride, dp_table_stride, grad_rows);
+    return launch_reduce_sgd(ts, T, d, dtype, nnz, B, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows,
+                             grad_rows ? grad_rows_cap : 0, workspace, vec, err_flag, st, eps, state);
+}
+
+int dlrm_emb_bag_reduce_adagrad(void *const *tables, float *const *state, const int64_t *rows, int T, int d,
+                                int dtype, int64_t nnz, int64_t B, const float *dpooled, int64_t dp_sample_stride,
+                                int64_t dp_table_stride, float lr, float eps, float *grad_rows,
+                                int64_t grad_rows_cap, void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                                dlrm_stream_t stream)
+{
+    TableSet ts;
+    int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
+    if (s != DLRM_OK)
+        return s;
+    if ((s = check_adagrad(state, T, d, lr, eps)) != DLRM_OK)
+        return s;
+    if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=
+        DLRM_OK)
+        return s;
+    if (B < 0 || nnz < 0 || (B == 0 && nnz != 0))
+        return DLRM_ERR_INVALID_ARG;
+    if (nnz > kMaxLookups || B > (int64_t)0x7fffffffLL)
+        return DLRM_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256))
+        return DLRM_ERR_INVALID_ARG;
+    if (workspace_bytes < emb_bag_bwd_workspace(T, nnz, d))
+        return DLRM_ERR_WORKSPACE_TOO_SMALL;
+    const bool vec = emb_bag_bwd_vectorisable(ts, T, d, dpooled, dp_sample_stride, dp_table_stride, grad_rows);
+    return launch_reduce_sgd(ts, T, d, dtype, nnz, B, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows,
+                             grad_rows ? grad_rows_cap : 0, workspace, vec, err_flag,
+                             static_cast<cudaStream_t>(stream), eps, state);
 }
 
 int dlrm_read_error(const int32_t *err_flag, dlrm_stream_t stream)

@@ -22,6 +22,8 @@
 //  6. reduce     per tile, the summed pooled gradient of every run of equal
 //                rows and the SGD update of its row (seg_reduce.cu)
 //  7. finalize   runs that cross chunk boundaries (seg_reduce.cu)
+#include <cstring>
+
 #include "emb_bag_bwd.cuh"
 
 namespace dlrm {
@@ -686,7 +688,7 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
 
 int launch_reduce_sgd(const TableSet &ts, int T, int d, int dtype, int64_t nnz, int64_t B, const float *dpooled,
                       int64_t dpss, int64_t dpts, float lr, float *grad_rows, int64_t grad_cap, void *workspace,
-                      bool vec, int32_t *err, cudaStream_t st)
+                      bool vec, int32_t *err, cudaStream_t st, float eps, float *const *state)
 {
     if (nnz == 0)
         return DLRM_OK;
@@ -707,6 +709,12 @@ int launch_reduce_sgd(const TableSet &ts, int T, int d, int dtype, int64_t nnz, 
     a.grad_cap = grad_cap;
     a.final_buf = final_buf;
     a.err = err;
+    a.opt = state ? kOptAdagrad : kOptSgd;
+    a.eps = eps;
+    std::memset(&a.state, 0, sizeof a.state);
+    if (state)
+        for (int t = 0; t < T; t++)
+            a.state.ptr[t] = state[t];
     return launch_seg_reduce(dtype, a, w, L.ntiles_max, vec, st);
 }
 
@@ -720,7 +728,7 @@ int launch_emb_bag_bwd(const TableSet &ts, int T, int d, int dtype, const int64_
     if (s != DLRM_OK)
         return s;
     return launch_reduce_sgd(ts, T, d, dtype, nnz, B, dpooled, dpss, dpts, lr, grad_rows, grad_cap, workspace,
-                             vec, err, st);
+                             vec, err, st, 0.f, nullptr);
 }
 
 }  // namespace dlrm

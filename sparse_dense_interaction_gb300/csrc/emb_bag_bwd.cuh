@@ -67,6 +67,15 @@ __device__ __forceinline__ bool run_starts(const uint32_t *skey, uint32_t j, uin
     return j == table_start || skey[j] != skey[j - 1];
 }
 
+// Optimizers of the update: plain SGD, or row-wise AdaGrad (one fp32
+// accumulator per row: s' = s + mean(g^2), w' = w - lr g / (sqrt(s') + eps)).
+constexpr int kOptSgd = 0, kOptAdagrad = 1;
+constexpr int kAdagradMaxD = 256;  // rows the AdaGrad update holds whole in registers
+
+struct StateSet {
+    float *ptr[DLRM_MAX_TABLES];  // accumulator of each row, per table (AdaGrad)
+};
+
 struct ReduceArgs {
     TableSet tables;  // written in place when lr != 0
     int T, d;
@@ -78,6 +87,9 @@ struct ReduceArgs {
     int64_t grad_cap;
     int final_buf;
     int32_t *err;
+    int opt;        // kOptSgd or kOptAdagrad
+    float eps;      // AdaGrad
+    StateSet state; // AdaGrad
 };
 
 // Segmented reduce + SGD and the combine of cross-chunk runs (seg_reduce.cu).

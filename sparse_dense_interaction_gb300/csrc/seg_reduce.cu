@@ -39,6 +39,11 @@ struct Vec<4> {
         a = make_float4(lo.x, lo.y, hi.x, hi.y);
     }
     __device__ __forceinline__ static float get(const F &v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+    // s + the squares of the four values
+    __device__ __forceinline__ static float sumsq(const F &v, float s)
+    {
+        return fmaf(v.w, v.w, fmaf(v.z, v.z, fmaf(v.y, v.y, fmaf(v.x, v.x, s))));
+    }
 };
 template <>
 struct Vec<1> {
@@ -48,6 +53,7 @@ struct Vec<1> {
     __device__ __forceinline__ static void store(float *p, const F &v) { *p = v; }
     __device__ __forceinline__ static void add(F &a, const F &b) { a += b; }
     __device__ __forceinline__ static float get(const F &v, int) { return v; }
+    __device__ __forceinline__ static float sumsq(const F &v, float s) { return fmaf(v, v, s); }
 };
 
 // VEC consecutive table elements of one lane.
@@ -121,6 +127,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
         key_after = ti.hi < te ? skey[ti.hi] : 0u;
     }
     const bool update = a.lr != 0.f;
+    const bool adagrad = a.opt == kOptAdagrad;
     TT *wtab = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t]));
     const int64_t rows_t = a.tables.rows[t];
 
@@ -185,6 +192,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     // B. one stream of G lanes per chunk
     const int sidx = warp * S + lane / G;
     const int gl = lane % G;
+    const unsigned smask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane / G * G));  // this stream's lanes
     const size_t ch = (size_t)blockIdx.x * NS + sidx;
     const uint32_t c0 = (uint32_t)sidx * CW;
     const uint32_t c1 = c0 + CW < n ? c0 + CW : n;
@@ -245,11 +253,28 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                         }
                     }
                     if (update && (int64_t)cur_row < rows_t) {
+                        float step = a.lr;
+                        if (adagrad) {
+                            // the whole row is in this stream's registers (d <= EB)
+                            float ss = 0.f;
+#pragma unroll
+                            for (int c = 0; c < C; c++)
+                                if (on[c])
+                                    ss = V::sumsq(acc[c], ss);
+#pragma unroll
+                            for (int o = G / 2; o > 0; o >>= 1)
+                                ss += __shfl_xor_sync(smask, ss, o);
+                            float *sp = a.state.ptr[t] + cur_row;
+                            const float s1 = *sp + ss / (float)a.d;
+                            step = a.lr / (sqrtf(s1) + a.eps);
+                            if (gl == 0)
+                                *sp = s1;
+                        }
 #pragma unroll
                         for (int c = 0; c < C; c++)
                             if (on[c]) {
                                 TT *wp = wtab + (int64_t)cur_row * a.d + eb + (c * G + gl) * VEC;
-                                RC::store(wp, RC::sgd(RC::load(wp), acc[c], a.lr));
+                                RC::store(wp, RC::sgd(RC::load(wp), acc[c], step));
                             }
                     }
                 }
@@ -273,6 +298,8 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                             for (int c = 0; c < C; c++)
                                 if (on[c])
                                     prefetch_l2(wr + c * G * VEC);
+                            if (adagrad && gl == 0)
+                                prefetch_l2(a.state.ptr[t] + kb.x);
                         }
                     }
                 }
@@ -392,7 +419,7 @@ seg_block_sum_kernel(ReduceArgs a, BwdPtrs w, int NS)
     }
 }
 
-template <typename TT, int VEC>
+template <typename TT, int VEC, int NB>
 __global__ void __launch_bounds__(256)
 seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
 {
@@ -434,6 +461,48 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
             if (endm)
                 ends = true;
         }
+        if (a.opt == kOptAdagrad) {
+            // the whole row (d <= NB * EB), then its sum of squares over the warp
+            F acc[NB];
+            float ss = 0.f;
+#pragma unroll
+            for (int nb = 0; nb < NB; nb++) {
+                const int e = nb * EB + lane * VEC;
+                acc[nb] = e < a.d ? V::load(w.tail + ch * a.d + e) : V::zero();
+                add_heads<VEC>(acc[nb], w.head, c1, count, a.d, e);
+                add_heads<VEC>(acc[nb], w.block_sum, first_blk, (int)nblocks_run, a.d, e);
+                ss = V::sumsq(acc[nb], ss);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const bool in_table = (int64_t)row < a.tables.rows[t];
+            float step = 0.f;
+            if (in_table && a.lr != 0.f) {
+                float *sp = a.state.ptr[t] + row;
+                const float s1 = *sp + ss / (float)a.d;
+                step = a.lr / (sqrtf(s1) + a.eps);
+                if (lane == 0)
+                    *sp = s1;
+            }
+#pragma unroll
+            for (int nb = 0; nb < NB; nb++) {
+                const int e = nb * EB + lane * VEC;
+                if (e >= a.d)
+                    continue;
+                if (a.grad_rows) {
+                    if ((int64_t)u < a.grad_cap)
+                        V::store(a.grad_rows + (int64_t)u * a.d + e, acc[nb]);
+                    else if (lane == 0 && nb == 0)
+                        raise_flag(a.err, DLRM_FLAG_CAPACITY);
+                }
+                if (in_table && a.lr != 0.f) {
+                    TT *wp = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t])) + (int64_t)row * a.d + e;
+                    RowChunk<TT, VEC>::store(wp, RowChunk<TT, VEC>::sgd(RowChunk<TT, VEC>::load(wp), acc[nb], step));
+                }
+            }
+            continue;
+        }
         for (int eb = 0; eb < a.d; eb += EB) {
             const int e = eb + lane * VEC;
             F acc = e < a.d ? V::load(w.tail + ch * a.d + e) : V::zero();
@@ -470,7 +539,8 @@ static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaS
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
-    seg_finalize_kernel<TT, VEC><<<(unsigned)((chunks + 7) / 8), 256, 0, st>>>(a, w, NS);
+    // AdaGrad holds whole rows: 2 x 128 (vectorised) or 8 x 32 (scalar) elements
+    seg_finalize_kernel<TT, VEC, kAdagradMaxD / (32 * VEC)><<<(unsigned)((chunks + 7) / 8), 256, 0, st>>>(a, w, NS);
     count_launch(st);
     return launch_status();
 }
@@ -478,8 +548,16 @@ static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaS
 template <typename TT>
 static int reduce_typed(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
 {
-    if (!vec)
+    if (a.opt == kOptAdagrad) {
+        // a stream holds the whole row: up to 128 (16 x 2 x 4 or 32 x 1 x 4),
+        // 256 (32 x 2 x 4) or 256 (32 x 8 x 1, scalar) elements
+        if (!vec)
+            return run_reduce<TT, 1, 32, 8, 2, 0>(a, w, grid, st);
+        if (a.d > 128)
+            return run_reduce<TT, 4, 32, 2, 2, 1>(a, w, grid, st);
+    } else if (!vec) {
         return run_reduce<TT, 1, 32, 1, 8, 0>(a, w, grid, st);
+    }
     // rows of 32+ pieces: half-warp streams with two pieces per lane
     return a.d >= 128 ? run_reduce<TT, 4, 16, 2, 2, 1>(a, w, grid, st) : run_reduce<TT, 4, 32, 1, 4, 1>(a, w, grid, st);
 }
