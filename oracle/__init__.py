@@ -142,20 +142,26 @@ def emb_bag_fwd(tables, dtype: str, offsets, indices, B: int):
     return pooled, mag
 
 
-def interact_fwd(e0, emb, include_self: bool, e0_mag=None, emb_mag=None):
-    """[e0 | pairwise dots] per sample: returns (y [B][d+P], magnitude)."""
+def interact_fwd(e0, emb, include_self: bool, e0_mag=None, emb_mag=None, alongside: bool = False):
+    """[e0 | pairwise dots] per sample, or [e0 | e_1 .. e_N | pairwise dots]
+    with ``alongside``: returns (y [B][width], magnitude)."""
     e0, emb = _f64(e0), _f64(emb)
     B, N, d = emb.shape
-    width = d + num_pairs(N, include_self)
+    width = d * (N + 1 if alongside else 1) + num_pairs(N, include_self)
     y = np.empty((B, width), dtype=np.float64)
     ym = np.empty_like(y)
-    _check(_load().oracle_interact_fwd(N, d, B, int(bool(include_self)), _ptr(e0),
+    _check(_load().oracle_interact_fwd(N, d, B, _mode(include_self, alongside), _ptr(e0),
                                        _ptr(_f64(e0_mag)), _ptr(emb), _ptr(_f64(emb_mag)),
                                        _ptr(y), _ptr(ym)), "interact_fwd")
     return y, ym
 
 
-def interact_bwd(e0, emb, dy, include_self: bool, e0_mag=None, emb_mag=None, dy_mag=None):
+def _mode(include_self, alongside):
+    return (1 if include_self else 0) | (2 if alongside else 0)
+
+
+def interact_bwd(e0, emb, dy, include_self: bool, e0_mag=None, emb_mag=None, dy_mag=None,
+                 alongside: bool = False):
     """Gradients of the interaction: returns (de0, de0_mag, demb, demb_mag)."""
     e0, emb, dy = _f64(e0), _f64(emb), _f64(dy)
     B, N, d = emb.shape
@@ -164,7 +170,7 @@ def interact_bwd(e0, emb, dy, include_self: bool, e0_mag=None, emb_mag=None, dy_
     demb = np.empty((B, N, d), dtype=np.float64)
     dembm = np.empty_like(demb)
     e0m, embm, dym = _f64(e0_mag), _f64(emb_mag), _f64(dy_mag)
-    _check(_load().oracle_interact_bwd(N, d, B, int(bool(include_self)), _ptr(e0), _ptr(e0m),
+    _check(_load().oracle_interact_bwd(N, d, B, _mode(include_self, alongside), _ptr(e0), _ptr(e0m),
                                        _ptr(emb), _ptr(embm), _ptr(dy), _ptr(dym),
                                        _ptr(de0), _ptr(de0m), _ptr(demb), _ptr(dembm)),
            "interact_bwd")

@@ -158,7 +158,18 @@ int oracle_emb_bag_fwd(int T, int d, int dtype, const void *const *tables, const
 int64_t oracle_num_pairs(int N, int include_self)
 {
     int64_t F = (int64_t)N + 1;
-    return include_self ? F * (F + 1) / 2 : F * (F - 1) / 2;
+    return (include_self & 1) ? F * (F + 1) / 2 : F * (F - 1) / 2;
+}
+
+/*
+ * Width of an interaction output row.  mode bit 0: self pairs; bit 1: the
+ * original embeddings are concatenated alongside (section 3 of the DLRM notes
+ * names this variant: "some include the original embeddings concatenated
+ * alongside the interaction vector"; read here as [e0 | e_1 .. e_N | pairs]).
+ */
+static int64_t interact_width(int N, int d, int mode)
+{
+    return (int64_t)d * ((mode & 2) ? N + 1 : 1) + oracle_num_pairs(N, mode & 1);
 }
 
 /*
@@ -171,7 +182,7 @@ int64_t oracle_num_pairs(int N, int include_self)
  * scalar dot product; e0 is placed first in the concatenation; pairs are
  * listed by row i, then column j.
  */
-int oracle_interact_fwd(int N, int d, int64_t B, int include_self,
+int oracle_interact_fwd(int N, int d, int64_t B, int mode,
                         const double *e0, const double *e0_mag,
                         const double *emb, const double *emb_mag,
                         double *y, double *y_mag)
@@ -179,7 +190,8 @@ int oracle_interact_fwd(int N, int d, int64_t B, int include_self,
     if (N < 0 || d <= 0 || B < 0)
         return ORACLE_INVALID_ARG;
     int F = N + 1;
-    int64_t width = d + oracle_num_pairs(N, include_self);
+    int include_self = mode & 1;
+    int64_t width = interact_width(N, d, mode);
     for (int64_t b = 0; b < B; b++) {
         double *yr = y + b * width;
         double *ym = y_mag + b * width;
@@ -188,6 +200,15 @@ int oracle_interact_fwd(int N, int d, int64_t B, int include_self,
             ym[e] = mag_or_abs(e0_mag, e0, b * d + e);
         }
         int64_t p = d;
+        if (mode & 2) { /* the original embeddings, in order */
+            for (int i = 0; i < N; i++)
+                for (int e = 0; e < d; e++) {
+                    int64_t k = (b * N + i) * (int64_t)d + e;
+                    yr[p] = emb[k];
+                    ym[p] = mag_or_abs(emb_mag, emb, k);
+                    p++;
+                }
+        }
         for (int i = 0; i < F; i++) {
             int jmax = include_self ? i : i - 1;
             for (int j = 0; j <= jmax; j++) {
@@ -218,7 +239,7 @@ int oracle_interact_fwd(int N, int d, int64_t B, int include_self,
  * 2 * g * z_i.  e0 also receives the gradient of its copy in the output.
  * de0 is [B][d]; demb is [B][N][d].
  */
-int oracle_interact_bwd(int N, int d, int64_t B, int include_self,
+int oracle_interact_bwd(int N, int d, int64_t B, int mode,
                         const double *e0, const double *e0_mag,
                         const double *emb, const double *emb_mag,
                         const double *dy, const double *dy_mag,
@@ -227,7 +248,8 @@ int oracle_interact_bwd(int N, int d, int64_t B, int include_self,
     if (N < 0 || d <= 0 || B < 0)
         return ORACLE_INVALID_ARG;
     int F = N + 1;
-    int64_t width = d + oracle_num_pairs(N, include_self);
+    int include_self = mode & 1;
+    int64_t width = interact_width(N, d, mode);
     double *dz = (double *)calloc((size_t)F * d, sizeof(double));
     double *dzm = (double *)calloc((size_t)F * d, sizeof(double));
     if (!dz || !dzm) {
@@ -238,7 +260,7 @@ int oracle_interact_bwd(int N, int d, int64_t B, int include_self,
     for (int64_t b = 0; b < B; b++) {
         memset(dz, 0, sizeof(double) * (size_t)F * d);
         memset(dzm, 0, sizeof(double) * (size_t)F * d);
-        int64_t p = d;
+        int64_t p = (mode & 2) ? (int64_t)F * d : d;
         for (int i = 0; i < F; i++) {
             int jmax = include_self ? i : i - 1;
             for (int j = 0; j <= jmax; j++) {
@@ -270,8 +292,14 @@ int oracle_interact_bwd(int N, int d, int64_t B, int include_self,
         }
         for (int i = 1; i < F; i++)
             for (int e = 0; e < d; e++) {
-                demb[(b * N + (i - 1)) * (int64_t)d + e] = dz[(int64_t)i * d + e];
-                demb_mag[(b * N + (i - 1)) * (int64_t)d + e] = dzm[(int64_t)i * d + e];
+                /* with the embeddings alongside, each also receives the gradient of its copy */
+                double cp = 0.0, cpm = 0.0;
+                if (mode & 2) {
+                    cp = dy[b * width + (int64_t)i * d + e];
+                    cpm = mag_or_abs(dy_mag, dy, b * width + (int64_t)i * d + e);
+                }
+                demb[(b * N + (i - 1)) * (int64_t)d + e] = cp + dz[(int64_t)i * d + e];
+                demb_mag[(b * N + (i - 1)) * (int64_t)d + e] = cpm + dzm[(int64_t)i * d + e];
             }
     }
     free(dz);

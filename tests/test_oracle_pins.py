@@ -475,3 +475,46 @@ def test_adagrad_zero_rate_and_zero_gradient():
     _, _, s, _, nr, _ = oracle.adagrad(tables, "f32", offsets, 1, 1, dp, 0.1, 1e-8, [2.0], co)
     assert s[0] == 2.0
     np.testing.assert_array_equal(nr[0], w[2])
+
+
+# -------------------------------------- original embeddings alongside ---
+
+@pytest.mark.parametrize("inc", [False, True])
+def test_alongside_output_is_e0_the_embeddings_then_the_pairs(inc):
+    # [e0 | e_1 .. e_N | pairs]: the copies are the inputs bit for bit and the
+    # pairs are those of the plain layout (pinned above by brute force and
+    # the factorization-machine identity)
+    rng = np.random.default_rng(21)
+    B, N, d = 3, 5, 4
+    e0 = rng.standard_normal((B, d))
+    emb = rng.standard_normal((B, N, d))
+    y, _ = oracle.interact_fwd(e0, emb, inc, alongside=True)
+    plain, _ = oracle.interact_fwd(e0, emb, inc)
+    assert y.shape == (B, d * (N + 1) + oracle.num_pairs(N, inc))
+    np.testing.assert_array_equal(y[:, :d], e0)
+    np.testing.assert_array_equal(y[:, d:d * (N + 1)], emb.reshape(B, N * d))
+    np.testing.assert_array_equal(y[:, d * (N + 1):], plain[:, d:])
+
+
+@pytest.mark.parametrize("inc", [False, True])
+def test_alongside_backward_by_finite_differences(inc):
+    rng = np.random.default_rng(22)
+    B, N, d = 2, 3, 3
+    e0 = rng.standard_normal((B, d))
+    emb = rng.standard_normal((B, N, d))
+    width = d * (N + 1) + oracle.num_pairs(N, inc)
+    w = rng.standard_normal((B, width))
+    de0, _, demb, _ = oracle.interact_bwd(e0, emb, w, inc, alongside=True)
+
+    def loss(a, b):
+        y, _ = oracle.interact_fwd(a, b, inc, alongside=True)
+        return float((w * y).sum())
+
+    h = 1e-3
+    for arr, grad, which in ((e0, de0, 0), (emb, demb, 1)):
+        for idx in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += h
+            m[idx] -= h
+            fd = ((loss(p, emb) - loss(m, emb)) if which == 0 else (loss(e0, p) - loss(e0, m))) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd))
