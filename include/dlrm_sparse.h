@@ -96,43 +96,64 @@ int dlrm_emb_bag_fwd(const void *const *tables, const int64_t *rows, int T, int 
  * Number of interaction terms over F = N + 1 vectors (e0 and N pooled
  * embeddings): F(F-1)/2 strict pairs, F(F+1)/2 with self pairs
  * ("Notes/DLRM", section 3; N(N+1)/2 there counts the strict pairs of
- * e0..eN).  Returns -1 if N < 0.
+ * e0..eN).  Bit 0 of include_self selects self pairs (a mode below may be
+ * passed).  Returns -1 if N < 0.
  */
 int64_t dlrm_num_pairs(int N, int include_self);
+
+/*
+ * Interaction modes (bits of the `mode` argument of the interaction calls).
+ * DLRM_INTERACT_SELF: self pairs z_i . z_i are included.
+ * DLRM_INTERACT_ALONGSIDE: the original embeddings are concatenated
+ *   alongside the interaction vector ("Notes/DLRM", section 3 names this
+ *   variant; its order is not given there): an output row is
+ *   [e0 | e_1 .. e_N | pairs] instead of [e0 | pairs].
+ */
+#define DLRM_INTERACT_SELF 1
+#define DLRM_INTERACT_ALONGSIDE 2
+
+/* Width of an interaction output row: d (or d (N + 1) alongside) plus the
+ * pairs.  Returns -1 for N < 0, d <= 0 or unknown mode bits. */
+int64_t dlrm_interact_width(int N, int d, int mode);
 
 /*
  * Interaction forward ("Notes/DLRM", section 3, and the architecture figure
  * of section 2).  With z_0 = e0[b] and z_i = emb[b][i-1] (i = 1..N):
  *
- *   y[b][0 .. d)      = e0[b]                    (the concatenated e0)
- *   y[b][d + p(i,j)]  = z_i . z_j   for j < i (strict) or j <= i (self pairs)
- *   p(i,j)            = i(i-1)/2 + j (strict),  i(i+1)/2 + j (self pairs)
+ *   y[b][0 .. d)       = e0[b]                    (the concatenated e0)
+ *   y[b][i*d .. i*d+d) = z_i, i = 1..N             (DLRM_INTERACT_ALONGSIDE only)
+ *   y[b][o + p(i,j)]   = z_i . z_j  for j < i, or j <= i with DLRM_INTERACT_SELF
+ *   p(i,j)             = i(i-1)/2 + j (strict),  i(i+1)/2 + j (self pairs)
+ *   o                  = d, or (N + 1) d alongside
  *
+ * mode  bits DLRM_INTERACT_SELF | DLRM_INTERACT_ALONGSIDE (0: strict pairs
+ *       after e0; 1 selects self pairs as a boolean did before).
  * e0    device fp32 rows of d, row stride e0_stride (elements).
  * emb   device fp32; pooled embedding i of sample b at
  *       emb[b*emb_sample_stride + i*d] (the [B][N][d] block of
  *       dlrm_emb_bag_fwd with out_table_stride = d).
- * y     device fp32 rows of d + dlrm_num_pairs(N, include_self), row stride
+ * y     device fp32 rows of dlrm_interact_width(N, d, mode), row stride
  *       y_stride.  N may be 0 .. 127.
  */
 int dlrm_interact_fwd(const float *e0, int64_t e0_stride, const float *emb,
-                      int64_t emb_sample_stride, int N, int d, int64_t B, int include_self,
+                      int64_t emb_sample_stride, int N, int d, int64_t B, int mode,
                       float *y, int64_t y_stride, dlrm_stream_t stream);
 
 /*
  * Interaction backward: the gradient of the forward above by the product
- * rule.  With G the F x F matrix holding dy[b][d + p(i,j)] at (i, j), j <= i,
+ * rule.  With G the F x F matrix holding dy[b][o + p(i,j)] at (i, j), j <= i,
  * and zero above the diagonal:
  *
  *   dZ        = (G + G^T) Z        (a self term contributes 2 g_ii z_i)
  *   de0[b]    = dy[b][0 .. d) + dZ[0]
  *   demb[b*demb_sample_stride + (i-1)*d + e] = dZ[i][e]     (i = 1..N)
+ *               + dy[b][i*d + e]   (alongside: the gradient of the copy)
  *
  * Inputs as in dlrm_interact_fwd; dy has row stride dy_stride, de0 row
  * stride de0_stride.  Outputs are overwritten (not accumulated).
  */
 int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb,
-                      int64_t emb_sample_stride, int N, int d, int64_t B, int include_self,
+                      int64_t emb_sample_stride, int N, int d, int64_t B, int mode,
                       const float *dy, int64_t dy_stride, float *de0, int64_t de0_stride,
                       float *demb, int64_t demb_sample_stride, dlrm_stream_t stream);
 
@@ -160,7 +181,7 @@ int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb,
  */
 int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, int T, int d, int dtype,
                               const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
-                              const float *e0, int64_t e0_stride, int include_self, float *y,
+                              const float *e0, int64_t e0_stride, int mode, float *y,
                               int64_t y_stride, float *pooled, int64_t pooled_sample_stride,
                               int64_t pooled_table_stride, int32_t *err_flag, dlrm_stream_t stream);
 

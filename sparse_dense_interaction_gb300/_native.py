@@ -38,6 +38,7 @@ SIGNATURES = {
     "dlrm_emb_bag_fwd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64, _i64,
                                 _vp, _vp]),
     "dlrm_num_pairs": (_i64, [_i32, _i32]),
+    "dlrm_interact_width": (_i64, [_i32, _i32, _i32]),
     "dlrm_interact_fwd": (_i32, [_vp, _i64, _vp, _i64, _i32, _i32, _i64, _i32, _vp, _i64, _vp]),
     "dlrm_interact_bwd": (_i32, [_vp, _i64, _vp, _i64, _i32, _i32, _i64, _i32, _vp, _i64, _vp,
                                  _i64, _vp, _i64, _vp]),
@@ -142,24 +143,36 @@ def dlrm_num_pairs(N: int, include_self: bool) -> int:
     return int(load().dlrm_num_pairs(N, int(bool(include_self))))
 
 
-def dlrm_interact_fwd(e0, emb, include_self: bool, y, stream=None):
+INTERACT_SELF, INTERACT_ALONGSIDE = 1, 2
+
+
+def _mode(include_self, alongside):
+    return (INTERACT_SELF if include_self else 0) | (INTERACT_ALONGSIDE if alongside else 0)
+
+
+def dlrm_interact_width(N: int, d: int, include_self: bool, alongside: bool = False) -> int:
+    """Width of an interaction output row: [e0 | pairs], or [e0 | e_1 .. e_N | pairs] alongside."""
+    return int(load().dlrm_interact_width(N, d, _mode(include_self, alongside)))
+
+
+def dlrm_interact_fwd(e0, emb, include_self: bool, y, stream=None, alongside: bool = False):
     """``y[b] = [e0[b] | z_i . z_j over pairs]`` for ``emb`` of shape [B][N][d]."""
     B, N, d = emb.shape
     if emb.stride(2) != 1 or emb.stride(1) != d or e0.stride(1) != 1 or y.stride(1) != 1:
         raise ValueError("rows must be contiguous and emb's tables adjacent")
     _check(load().dlrm_interact_fwd(e0.data_ptr(), e0.stride(0), emb.data_ptr(), emb.stride(0), N, d,
-                                    B, int(bool(include_self)), y.data_ptr(), y.stride(0),
+                                    B, _mode(include_self, alongside), y.data_ptr(), y.stride(0),
                                     _stream(stream)), "dlrm_interact_fwd")
 
 
-def dlrm_interact_bwd(e0, emb, include_self: bool, dy, de0, demb, stream=None):
+def dlrm_interact_bwd(e0, emb, include_self: bool, dy, de0, demb, stream=None, alongside: bool = False):
     """Gradients of :func:`dlrm_interact_fwd` into ``de0`` [B][d] and ``demb`` [B][N][d]."""
     B, N, d = emb.shape
     for t in (emb, demb):
         if t.stride(2) != 1 or t.stride(1) != d:
             raise ValueError("rows must be contiguous and tables adjacent")
     _check(load().dlrm_interact_bwd(e0.data_ptr(), e0.stride(0), emb.data_ptr(), emb.stride(0), N, d,
-                                    B, int(bool(include_self)), dy.data_ptr(), dy.stride(0),
+                                    B, _mode(include_self, alongside), dy.data_ptr(), dy.stride(0),
                                     de0.data_ptr(), de0.stride(0), demb.data_ptr(), demb.stride(0),
                                     _stream(stream)), "dlrm_interact_bwd")
 
@@ -239,7 +252,7 @@ def dlrm_emb_bag_reduce_sgd(tables, nnz: int, B: int, dpooled, lr: float, worksp
 
 
 def dlrm_emb_bag_interact_fwd(tables, offsets, indices, B: int, e0, include_self: bool, y, pooled=None,
-                              err_flag=None, stream=None):
+                              err_flag=None, stream=None, alongside: bool = False):
     """Lookup + interaction forward in one call: ``y`` ([B][d + P] fp32, last
     dim 1) receives what :func:`dlrm_interact_fwd` would give on the pooled
     vectors of :func:`dlrm_emb_bag_fwd`; ``pooled`` ([B][T][d] fp32, optional)
@@ -254,7 +267,7 @@ def dlrm_emb_bag_interact_fwd(tables, offsets, indices, B: int, e0, include_self
         pss, pts = pooled.stride(0), pooled.stride(1)
     _check(load().dlrm_emb_bag_interact_fwd(ptrs, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices),
                                             indices.numel(), B, e0.data_ptr(), e0.stride(0),
-                                            1 if include_self else 0, y.data_ptr(), y.stride(0), _ptr(pooled),
+                                            _mode(include_self, alongside), y.data_ptr(), y.stride(0), _ptr(pooled),
                                             pss, pts, _ptr(err_flag), _stream(stream)),
            "dlrm_emb_bag_interact_fwd")
 

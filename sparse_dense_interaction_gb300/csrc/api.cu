@@ -125,7 +125,7 @@ int64_t dlrm_num_pairs(int N, int include_self)
     if (N < 0)
         return -1;
     const int64_t F = (int64_t)N + 1;
-    return include_self ? F * (F + 1) / 2 : F * (F - 1) / 2;
+    return (include_self & DLRM_INTERACT_SELF) ? F * (F + 1) / 2 : F * (F - 1) / 2;
 }
 
 static int check_interact(const float *e0, int64_t e0_stride, const float *emb, int64_t emb_sample_stride,
@@ -142,30 +142,40 @@ static int check_interact(const float *e0, int64_t e0_stride, const float *emb, 
     return DLRM_OK;
 }
 
+int64_t dlrm_interact_width(int N, int d, int mode)
+{
+    if (N < 0 || d <= 0 || (mode & ~(DLRM_INTERACT_SELF | DLRM_INTERACT_ALONGSIDE)))
+        return -1;
+    return (int64_t)d * ((mode & DLRM_INTERACT_ALONGSIDE) ? (int64_t)N + 1 : 1) +
+           dlrm_num_pairs(N, mode & DLRM_INTERACT_SELF);
+}
+
 int dlrm_interact_fwd(const float *e0, int64_t e0_stride, const float *emb, int64_t emb_sample_stride,
-                      int N, int d, int64_t B, int include_self, float *y, int64_t y_stride,
+                      int N, int d, int64_t B, int mode, float *y, int64_t y_stride,
                       dlrm_stream_t stream)
 {
     int s = check_interact(e0, e0_stride, emb, emb_sample_stride, N, d, B);
     if (s != DLRM_OK)
         return s;
-    if (y_stride < d + dlrm_num_pairs(N, include_self) || (B > 0 && !y) || !aligned(y, 4))
+    const int64_t width = dlrm_interact_width(N, d, mode);
+    if (width < 0 || y_stride < width || (B > 0 && !y) || !aligned(y, 4))
         return DLRM_ERR_INVALID_ARG;
     if (B == 0)
         return DLRM_OK;
-    return launch_interact_fwd(e0, e0_stride, emb, emb_sample_stride, N, d, B, include_self ? 1 : 0, y,
-                               y_stride, static_cast<cudaStream_t>(stream));
+    return launch_interact_fwd(e0, e0_stride, emb, emb_sample_stride, N, d, B, mode, y, y_stride,
+                               static_cast<cudaStream_t>(stream));
 }
 
 int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb, int64_t emb_sample_stride,
-                      int N, int d, int64_t B, int include_self, const float *dy, int64_t dy_stride,
+                      int N, int d, int64_t B, int mode, const float *dy, int64_t dy_stride,
                       float *de0, int64_t de0_stride, float *demb, int64_t demb_sample_stride,
                       dlrm_stream_t stream)
 {
     int s = check_interact(e0, e0_stride, emb, emb_sample_stride, N, d, B);
     if (s != DLRM_OK)
         return s;
-    if (dy_stride < d + dlrm_num_pairs(N, include_self) || de0_stride < d ||
+    const int64_t width = dlrm_interact_width(N, d, mode);
+    if (width < 0 || dy_stride < width || de0_stride < d ||
         (N > 0 && demb_sample_stride < (int64_t)N * d))
         return DLRM_ERR_INVALID_ARG;
     if (B > 0 && (!dy || !de0 || (N > 0 && !demb)))
@@ -174,14 +184,14 @@ int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb, int6
         return DLRM_ERR_INVALID_ARG;
     if (B == 0)
         return DLRM_OK;
-    return launch_interact_bwd(e0, e0_stride, emb, emb_sample_stride, N, d, B, include_self ? 1 : 0, dy,
+    return launch_interact_bwd(e0, e0_stride, emb, emb_sample_stride, N, d, B, mode, dy,
                                dy_stride, de0, de0_stride, demb, demb_sample_stride,
                                static_cast<cudaStream_t>(stream));
 }
 
 int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, int T, int d, int dtype,
                               const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
-                              const float *e0, int64_t e0_stride, int include_self, float *y, int64_t y_stride,
+                              const float *e0, int64_t e0_stride, int mode, float *y, int64_t y_stride,
                               float *pooled, int64_t pooled_sample_stride, int64_t pooled_table_stride,
                               int32_t *err_flag, dlrm_stream_t stream)
 {
@@ -189,7 +199,8 @@ int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, in
     int s = make_tables(tables, rows, T, d, dtype, ts);
     if (s != DLRM_OK)
         return s;
-    if (B < 0 || nnz < 0 || e0_stride < d || y_stride < d + dlrm_num_pairs(T, include_self))
+    const int64_t width = dlrm_interact_width(T, d, mode);
+    if (B < 0 || nnz < 0 || e0_stride < d || width < 0 || y_stride < width)
         return DLRM_ERR_INVALID_ARG;
     if (pooled && (pooled_sample_stride < 0 || pooled_table_stride < 0))
         return DLRM_ERR_INVALID_ARG;
@@ -202,7 +213,6 @@ int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, in
     if (!aligned(offsets, 8) || (indices && !aligned(indices, 8)) || !aligned(e0, 4) || !aligned(y, 4) ||
         (pooled && !aligned(pooled, 4)))
         return DLRM_ERR_INVALID_ARG;
-    const int inc = include_self ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t row_bytes = (int64_t)d * elem_bytes(dtype);
     bool fused = row_bytes % 16 == 0 && row_bytes <= 1024;
@@ -211,8 +221,8 @@ int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, in
     if (pooled)
         fused = fused && aligned(pooled, 16) && pooled_sample_stride % 4 == 0 && pooled_table_stride % 4 == 0;
     FusedShape fs;
-    if (fused && emb_bag_interact_shape(T, d, inc, B, fs))
-        return launch_emb_bag_interact_fwd(ts, T, d, dtype, offsets, indices, nnz, B, e0, e0_stride, inc, y,
+    if (fused && emb_bag_interact_shape(T, d, mode & DLRM_INTERACT_SELF, B, fs))
+        return launch_emb_bag_interact_fwd(ts, T, d, dtype, offsets, indices, nnz, B, e0, e0_stride, mode, y,
                                            y_stride, pooled, pooled_sample_stride, pooled_table_stride, fs,
                                            err_flag, st);
     // the two calls it fuses, through the caller's pooled block
@@ -224,7 +234,7 @@ int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, in
                            pooled_table_stride, err_flag, st);
     if (s != DLRM_OK)
         return s;
-    return launch_interact_fwd(e0, e0_stride, pooled, pooled_sample_stride, T, d, B, inc, y, y_stride, st);
+    return launch_interact_fwd(e0, e0_stride, pooled, pooled_sample_stride, T, d, B, mode, y, y_stride, st);
 }
 
 size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d)

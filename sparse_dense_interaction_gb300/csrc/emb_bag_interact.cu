@@ -31,7 +31,7 @@ template <typename TT, int G, int C, int U>
 __global__ void __launch_bounds__(256, 4)
 emb_bag_interact_fwd_kernel(TableSet ts, int T, int d, int nchunks, const int64_t *__restrict__ offsets,
                             const int64_t *__restrict__ indices, int64_t nnz, int64_t B,
-                            const float *__restrict__ e0, int64_t e0s, int inc, float *__restrict__ y,
+                            const float *__restrict__ e0, int64_t e0s, int mode, float *__restrict__ y,
                             int64_t ys, float *__restrict__ pooled, int64_t pss, int64_t pts, int S, int KS,
                             int32_t *err)
 {
@@ -39,6 +39,8 @@ emb_bag_interact_fwd_kernel(TableSet ts, int T, int d, int nchunks, const int64_
     constexpr int EPC = Chunk16<TT>::kElems;  // elements per 16-byte chunk
     constexpr uint32_t kBad = 0xffffffffu;    // row slot without a valid lookup
     static_assert(U <= G && G % U == 0, "a group walks its G indices in steps of U");
+    const int inc = mode & kInteractSelf;
+    const bool along = (mode & kInteractAlongside) != 0;
     const int F = T + 1;
     const int Fp = (F + 3) & ~3;
     const int TS = (Fp + 31) & ~31;  // staged row of Zt: Fp columns, swizzled
@@ -144,6 +146,14 @@ emb_bag_interact_fwd_kernel(TableSet ts, int T, int d, int nchunks, const int64_
                         __stcs(dst + q, make_float4(acc[c][2 * q].x, acc[c][2 * q].y, acc[c][2 * q + 1].x,
                                                     acc[c][2 * q + 1].y));
                 }
+                if (along) {  // the pooled vector alongside, in column block t + 1 of y
+                    float *dst = y + b * ys + (int64_t)(t + 1) * d + e;
+#pragma unroll
+                    for (int m = 0; m < EPC / 2; m++) {
+                        __stcs(dst + 2 * m, acc[c][m].x);
+                        __stcs(dst + 2 * m + 1, acc[c][m].y);
+                    }
+                }
             }
         }
     }
@@ -213,7 +223,7 @@ emb_bag_interact_fwd_kernel(TableSet ts, int T, int d, int nchunks, const int64_
     for (int64_t li = tid; li < (int64_t)nS * P; li += blockDim.x) {
         const int ss = (int)(li / P);
         const int64_t p = li - (int64_t)ss * P;
-        __stcs(y + (b0 + ss) * ys + d + p, ybuf[li]);
+        __stcs(y + (b0 + ss) * ys + (along ? (int64_t)F * d : d) + p, ybuf[li]);
     }
 }
 
@@ -256,7 +266,7 @@ bool emb_bag_interact_shape(int T, int d, int inc, int64_t B, FusedShape &fs)
 
 template <typename TT, int G, int C>
 static int launch_fused(const TableSet &ts, int T, int d, int nchunks, const int64_t *offsets,
-                        const int64_t *indices, int64_t nnz, int64_t B, const float *e0, int64_t e0s, int inc,
+                        const int64_t *indices, int64_t nnz, int64_t B, const float *e0, int64_t e0s, int mode,
                         float *y, int64_t ys, float *pooled, int64_t pss, int64_t pts, const FusedShape &fs,
                         int32_t *err, cudaStream_t st)
 {
@@ -269,49 +279,49 @@ static int launch_fused(const TableSet &ts, int T, int d, int nchunks, const int
         attr_set = true;
     }
     const int64_t grid = (B + fs.S - 1) / fs.S;
-    kernel<<<(unsigned)grid, fs.threads, fs.smem, st>>>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, inc,
-                                                        y, ys, pooled, pss, pts, fs.S, fs.KS, err);
+    kernel<<<(unsigned)grid, fs.threads, fs.smem, st>>>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s,
+                                                        mode, y, ys, pooled, pss, pts, fs.S, fs.KS, err);
     count_launch(st);
     return launch_status();
 }
 
 template <typename TT>
 static int fused_typed(const TableSet &ts, int T, int d, const int64_t *offsets, const int64_t *indices,
-                       int64_t nnz, int64_t B, const float *e0, int64_t e0s, int inc, float *y, int64_t ys,
+                       int64_t nnz, int64_t B, const float *e0, int64_t e0s, int mode, float *y, int64_t ys,
                        float *pooled, int64_t pss, int64_t pts, const FusedShape &fs, int32_t *err,
                        cudaStream_t st)
 {
     const int nchunks = (int)((int64_t)d * sizeof(TT) / 16);
     if (nchunks <= 4)
-        return launch_fused<TT, 4, 1>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, inc, y, ys, pooled,
+        return launch_fused<TT, 4, 1>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, mode, y, ys, pooled,
                                       pss, pts, fs, err, st);
     if (nchunks <= 8)
-        return launch_fused<TT, 8, 1>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, inc, y, ys, pooled,
+        return launch_fused<TT, 8, 1>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, mode, y, ys, pooled,
                                       pss, pts, fs, err, st);
     if (nchunks <= 16)
-        return launch_fused<TT, 16, 1>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, inc, y, ys, pooled,
+        return launch_fused<TT, 16, 1>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, mode, y, ys, pooled,
                                        pss, pts, fs, err, st);
     if (nchunks <= 32)
-        return launch_fused<TT, 32, 1>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, inc, y, ys, pooled,
+        return launch_fused<TT, 32, 1>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, mode, y, ys, pooled,
                                        pss, pts, fs, err, st);
-    return launch_fused<TT, 32, 2>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, inc, y, ys, pooled, pss,
+    return launch_fused<TT, 32, 2>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s, mode, y, ys, pooled, pss,
                                    pts, fs, err, st);
 }
 
 int launch_emb_bag_interact_fwd(const TableSet &ts, int T, int d, int dtype, const int64_t *offsets,
                                 const int64_t *indices, int64_t nnz, int64_t B, const float *e0, int64_t e0s,
-                                int inc, float *y, int64_t ys, float *pooled, int64_t pss, int64_t pts,
+                                int mode, float *y, int64_t ys, float *pooled, int64_t pss, int64_t pts,
                                 const FusedShape &fs, int32_t *err, cudaStream_t st)
 {
     switch (dtype) {
     case DLRM_F32:
-        return fused_typed<float>(ts, T, d, offsets, indices, nnz, B, e0, e0s, inc, y, ys, pooled, pss, pts, fs,
+        return fused_typed<float>(ts, T, d, offsets, indices, nnz, B, e0, e0s, mode, y, ys, pooled, pss, pts, fs,
                                   err, st);
     case DLRM_F16:
-        return fused_typed<__half>(ts, T, d, offsets, indices, nnz, B, e0, e0s, inc, y, ys, pooled, pss, pts, fs,
+        return fused_typed<__half>(ts, T, d, offsets, indices, nnz, B, e0, e0s, mode, y, ys, pooled, pss, pts, fs,
                                    err, st);
     default:
-        return fused_typed<__nv_bfloat16>(ts, T, d, offsets, indices, nnz, B, e0, e0s, inc, y, ys, pooled, pss,
+        return fused_typed<__nv_bfloat16>(ts, T, d, offsets, indices, nnz, B, e0, e0s, mode, y, ys, pooled, pss,
                                           pts, fs, err, st);
     }
 }

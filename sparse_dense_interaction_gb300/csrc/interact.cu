@@ -44,11 +44,14 @@ __device__ __forceinline__ void load8(const float *src, int k, int d, bool vec, 
 
 __global__ void __launch_bounds__(1024)
 interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__restrict__ emb,
-                    int64_t embs, int N, int d, int64_t B, int inc, float *__restrict__ y,
+                    int64_t embs, int N, int d, int64_t B, int mode, float *__restrict__ y,
                     int64_t ys, int S, int vec_in, int vec_out)
 {
     extern __shared__ __align__(16) float smem[];
+    const int inc = mode & kInteractSelf;
+    const bool along = (mode & kInteractAlongside) != 0;
     const int F = N + 1;
+    const int64_t poff = along ? (int64_t)F * d : d;  // first pair column
     const int Fp = (F + 3) & ~3;
     const int TS = (Fp + 31) & ~31;                     // staged row: Fp columns, swizzled
     const int nTR = Fp / 4;
@@ -91,8 +94,8 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
             if (b < B && k < d) {
                 const float *src = (i == 0) ? e0 + b * e0s : emb + b * embs + (int64_t)(i - 1) * d;
                 load8(src, k, d, vec_in != 0, v);
-                if (i == 0) {
-                    float *dst = y + b * ys + k;
+                if (i == 0 || along) {  // e0, and the embeddings when they go alongside
+                    float *dst = y + b * ys + (int64_t)i * d + k;
                     if (vec_y && k + 8 <= d) {
                         __stcs(reinterpret_cast<float4 *>(dst), make_float4(v[0], v[1], v[2], v[3]));
                         __stcs(reinterpret_cast<float4 *>(dst + 4), make_float4(v[4], v[5], v[6], v[7]));
@@ -152,18 +155,21 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
         const int64_t p = li - (int64_t)ss * P;
         const int64_t b = b0 + ss;
         if (b < B)
-            __stcs(y + b * ys + d + p, ybuf[li]);
+            __stcs(y + b * ys + poff + p, ybuf[li]);
     }
 }
 
 __global__ void __launch_bounds__(1024)
 interact_bwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__restrict__ emb,
-                    int64_t embs, int N, int d, int64_t B, int inc, const float *__restrict__ dy,
+                    int64_t embs, int N, int d, int64_t B, int mode, const float *__restrict__ dy,
                     int64_t dys, float *__restrict__ de0, int64_t de0s, float *__restrict__ demb,
                     int64_t dembs, int S, int vec_in, int vec_out)
 {
     extern __shared__ __align__(16) float smem[];
+    const int inc = mode & kInteractSelf;
+    const bool along = (mode & kInteractAlongside) != 0;
     const int F = N + 1;
+    const int64_t poff = along ? (int64_t)F * d : d;  // first pair column of dy
     const int Fp = (F + 3) & ~3;
     const int nTR = Fp / 4;
     constexpr int KQ = kKC / 4;
@@ -180,7 +186,7 @@ interact_bwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
         const int64_t b = b0 + ss;
         float g = 0.f;
         if (b < B && i < F && j < F) {
-            const float *row = dy + b * dys + d;
+            const float *row = dy + b * dys + poff;
             if (i > j)
                 g = row[pair_pos(i, j, inc)];
             else if (i < j)
@@ -250,15 +256,16 @@ interact_bwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
                         continue;
                     float out[4] = {acc[r][0], acc[r][1], acc[r][2], acc[r][3]};
                     float *dst;
-                    if (i == 0) {
-                        const float *dyr = dy + b * dys + k;
+                    if (i == 0 || along) {  // the gradient of the copy in the output
+                        const float *dyr = dy + b * dys + (int64_t)i * d + k;
                         for (int c = 0; c < 4; c++)
                             if (k + c < d)
                                 out[c] += __ldg(dyr + c);
-                        dst = de0 + b * de0s + k;
-                    } else {
-                        dst = demb + b * dembs + (int64_t)(i - 1) * d + k;
                     }
+                    if (i == 0)
+                        dst = de0 + b * de0s + k;
+                    else
+                        dst = demb + b * dembs + (int64_t)(i - 1) * d + k;
                     if (full) {
                         __stcs(reinterpret_cast<float4 *>(dst), make_float4(out[0], out[1], out[2], out[3]));
                     } else {
@@ -276,8 +283,9 @@ interact_bwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
 static bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
 int launch_interact_fwd(const float *e0, int64_t e0s, const float *emb, int64_t embs, int N, int d,
-                        int64_t B, int inc, float *y, int64_t ys, cudaStream_t st)
+                        int64_t B, int mode, float *y, int64_t ys, cudaStream_t st)
 {
+    const int inc = mode & kInteractSelf;
     const int F = N + 1;
     const int Fp = (F + 3) & ~3;
     const int nTR = Fp / 4;
@@ -300,14 +308,14 @@ int launch_interact_fwd(const float *e0, int64_t e0s, const float *emb, int64_t 
     const int vec_in = d % 4 == 0 && aligned16(e0) && aligned16(emb) && e0s % 4 == 0 && embs % 4 == 0;
     const int vec_out = aligned16(y) && ys % 4 == 0;
     const int64_t grid = (B + S - 1) / S;
-    interact_fwd_kernel<<<(unsigned)grid, threads, smem, st>>>(e0, e0s, emb, embs, N, d, B, inc, y, ys,
+    interact_fwd_kernel<<<(unsigned)grid, threads, smem, st>>>(e0, e0s, emb, embs, N, d, B, mode, y, ys,
                                                                S, vec_in, vec_out);
     count_launch(st);
     return launch_status();
 }
 
 int launch_interact_bwd(const float *e0, int64_t e0s, const float *emb, int64_t embs, int N, int d,
-                        int64_t B, int inc, const float *dy, int64_t dys, float *de0, int64_t de0s,
+                        int64_t B, int mode, const float *dy, int64_t dys, float *de0, int64_t de0s,
                         float *demb, int64_t dembs, cudaStream_t st)
 {
     const int F = N + 1;
@@ -330,7 +338,7 @@ int launch_interact_bwd(const float *e0, int64_t e0s, const float *emb, int64_t 
     const int vec_in = d % 4 == 0 && aligned16(e0) && aligned16(emb) && e0s % 4 == 0 && embs % 4 == 0;
     const int vec_out = d % 4 == 0 && aligned16(de0) && aligned16(demb) && de0s % 4 == 0 && dembs % 4 == 0;
     const int64_t grid = (B + S - 1) / S;
-    interact_bwd_kernel<<<(unsigned)grid, threads, smem, st>>>(e0, e0s, emb, embs, N, d, B, inc, dy, dys,
+    interact_bwd_kernel<<<(unsigned)grid, threads, smem, st>>>(e0, e0s, emb, embs, N, d, B, mode, dy, dys,
                                                                de0, de0s, demb, dembs, S, vec_in, vec_out);
     count_launch(st);
     return launch_status();

@@ -7,6 +7,10 @@ namespace dlrm {
 
 constexpr int kKC = 32;  // columns of Z per shared-memory chunk
 
+// Bits of the interaction mode: self pairs; the original embeddings
+// concatenated alongside, [e0 | e_1 .. e_N | pairs] (else [e0 | pairs]).
+constexpr int kInteractSelf = 1, kInteractAlongside = 2;
+
 // Output position of the pair (i, j), j < i (strict) or j <= i (self pairs):
 // rows of the lower triangle in order, i ascending, then j ascending.
 __device__ __forceinline__ int64_t pair_pos(int i, int j, int inc)

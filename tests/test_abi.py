@@ -98,6 +98,12 @@ def test_interaction_rejects_bad_arguments(lib):
     assert fwd(ys=8 + 10 - 1) == _native.ERR_INVALID_ARG  # width d + P = 18
     assert fwd(y=None) == _native.ERR_INVALID_ARG
     assert fwd(B=0) == _native.OK
+    # the mode's unknown bits, and the alongside width (d (N + 1) + P = 40 + 10)
+    mfwd = lambda mode, ys: lib.dlrm_interact_fwd(FAKE, 8, FAKE, 32, 4, 8, 2, mode, FAKE, ys, None)
+    assert mfwd(4, 1000) == _native.ERR_INVALID_ARG
+    assert mfwd(2, 49) == _native.ERR_INVALID_ARG
+    assert lib.dlrm_interact_width(4, 8, 2) == 50 and lib.dlrm_interact_width(4, 8, 3) == 55
+    assert lib.dlrm_interact_width(4, 8, 8) == -1
     bwd = lambda dys=18, de0s=8: lib.dlrm_interact_bwd(FAKE, 8, FAKE, 32, 4, 8, 2, 0, FAKE, dys, FAKE,
                                                        de0s, FAKE, 32, None)
     assert bwd(dys=17) == _native.ERR_INVALID_ARG

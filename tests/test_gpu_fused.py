@@ -135,3 +135,21 @@ def test_fused_empty_bags_and_out_of_range_index():
     y_ref, y_mag = oracle.interact_fwd(e0, p_ref, False, emb_mag=p_mag)
     assert_close(y.cpu().numpy(), y_ref, y_mag, REL["f32"], "empty/oob")
     assert np.all(y.cpu().numpy()[0, 16:] == 0.0)  # sample 0: both bags empty, every product zero
+
+
+@pytest.mark.parametrize("case", ["multi-hot-f16", "T40-self-d64", "tiny"])
+def test_fused_alongside_matches_oracle(case):
+    cfg = _cfg(case)
+    host, tables, offsets, indices, e0 = _inputs(cfg)
+    B, T, d, inc = cfg["B"], cfg["T"], cfg["d"], cfg["include_self"]
+    width = sdi.dlrm_interact_width(T, d, inc, alongside=True)
+    y = torch.full((B, width), float("nan"), device=DEV)
+    sdi.dlrm_emb_bag_interact_fwd(tables, _t(offsets), _t(indices), B, _t(e0), inc, y, alongside=True)
+    p_ref, p_mag = oracle.emb_bag_fwd(host, cfg["dtype"], offsets, indices, B)
+    y_ref, y_mag = oracle.interact_fwd(e0, p_ref, inc, emb_mag=p_mag, alongside=True)
+    assert_close(y.cpu().numpy(), y_ref, y_mag, REL[cfg["dtype"]], f"fused alongside {case}")
+    # the copies are the pooled vectors of the standalone lookup, bit for bit
+    alone = torch.empty((B, T, d), device=DEV)
+    sdi.dlrm_emb_bag_fwd(tables, _t(offsets), _t(indices), B, alone)
+    np.testing.assert_array_equal(y[:, d:d * (T + 1)].cpu().numpy().view(np.uint32),
+                                  alone.reshape(B, T * d).cpu().numpy().view(np.uint32))

@@ -183,6 +183,34 @@ def test_interact_with_padded_rows():
     assert torch.all(y_big[:, d + P:] == -1.0)
 
 
+ALONG_CASES = [(300, 26, 128, False), (37, 100, 256, True), (65, 5, 3, False), (21, 13, 33, True),
+               (50, 0, 16, True), (33, 1, 8, False)]
+
+
+@pytest.mark.parametrize("B,N,d,inc", ALONG_CASES)
+def test_interact_alongside_matches_oracle(B, N, d, inc):
+    # [e0 | e_1 .. e_N | pairs]: forward and backward
+    rng = np.random.default_rng([7, B, N, d, inc])
+    e0 = rng.standard_normal((B, d), dtype=np.float32)
+    emb = rng.standard_normal((B, N, d), dtype=np.float32)
+    width = sdi.dlrm_interact_width(N, d, inc, alongside=True)
+    assert width == d * (N + 1) + oracle.num_pairs(N, inc)
+    dy = rng.standard_normal((B, width), dtype=np.float32)
+    emb_t = _t(emb) if N else torch.empty((B, 0, d), device=DEV)
+    y = torch.full((B, width), float("nan"), device=DEV)
+    sdi.dlrm_interact_fwd(_t(e0), emb_t, inc, y, alongside=True)
+    ref, mag = oracle.interact_fwd(e0, emb, inc, alongside=True)
+    got = y.cpu().numpy()
+    np.testing.assert_array_equal(got[:, :d * (N + 1)], ref[:, :d * (N + 1)])  # the copies
+    assert_close(got, ref, mag, REL["f32"], f"alongside fwd B={B} N={N} d={d}")
+    de0 = torch.full((B, d), float("nan"), device=DEV)
+    demb = torch.full((B, N, d), float("nan"), device=DEV)
+    sdi.dlrm_interact_bwd(_t(e0), emb_t, inc, _t(dy), de0, demb, alongside=True)
+    r_de0, m_de0, r_demb, m_demb = oracle.interact_bwd(e0, emb, dy, inc, alongside=True)
+    assert_close(de0.cpu().numpy(), r_de0, m_de0, REL["f32"], "alongside de0")
+    assert_close(demb.cpu().numpy(), r_demb, m_demb, REL["f32"], "alongside demb")
+
+
 # -------------------------------------------------------- backward + SGD ---
 
 BWD_CASES = {
