@@ -29,8 +29,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "dlrm_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 
-F32, F16, BF16 = 0, 1, 2
-_DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16}
+F32, F16, BF16, INT4 = 0, 1, 2, 3
+_DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16, "int4": INT4}
 
 OK, INVALID_ARG, INDEX_OOB, BAD_OFFSETS, NO_MEMORY = 0, -1, -4, -5, -8
 
@@ -74,10 +74,14 @@ def _load():
             lib.oracle_coalesce.argtypes = [i32, i64, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp]
             lib.oracle_sgd.argtypes = [i32, i32, i32, vp, vp, i64, vp, i64, dp, dp,
                                        ctypes.c_double, vp, vp, vp, vp, i64, dp, dp, dp, dp]
+            lib.oracle_quantize_int4.argtypes = [i64, i32, i32, vp, vp]
+            lib.oracle_int4_row_bytes.argtypes = [i32]
+            lib.oracle_int4_row_bytes.restype = i64
             lib.oracle_adagrad.argtypes = [i32, i32, i32, vp, vp, i64, vp, i64, dp, dp, ctypes.c_double,
                                            ctypes.c_double, vp, vp, vp, vp, i64, dp, dp, dp, dp, dp, dp, dp]
             for name in ("oracle_decode", "oracle_emb_bag_fwd", "oracle_interact_fwd",
-                         "oracle_interact_bwd", "oracle_coalesce", "oracle_sgd", "oracle_adagrad"):
+                         "oracle_interact_bwd", "oracle_coalesce", "oracle_sgd", "oracle_adagrad",
+                         "oracle_quantize_int4"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -101,9 +105,12 @@ def _check(status: int, what: str):
 
 
 def _table_bits(table: np.ndarray, dtype: str) -> np.ndarray:
-    """Storage of one table for the C side: float32, or the 16-bit patterns."""
+    """Storage of one table for the C side: float32, the 16-bit patterns, or
+    the bytes of an int4 table ([rows][int4_row_bytes(d)] uint8)."""
     if dtype == "f32":
         return np.ascontiguousarray(table, dtype=np.float32)
+    if dtype == "int4":
+        return np.ascontiguousarray(table, dtype=np.uint8)
     if table.dtype == np.float16:
         return np.ascontiguousarray(table).view(np.uint16)
     return np.ascontiguousarray(table, dtype=np.uint16)
@@ -129,10 +136,27 @@ def _tables_arg(tables, dtype):
     return held, arr, rows
 
 
-def emb_bag_fwd(tables, dtype: str, offsets, indices, B: int):
-    """Sum-pooled lookups: returns (pooled [B][T][d], magnitude) in fp64."""
+def int4_row_bytes(d: int) -> int:
+    """Bytes of one row of an int4 table: d/2 code bytes, fp32 scale and bias, padded to 16."""
+    return int(_load().oracle_int4_row_bytes(d))
+
+
+def quantize_int4(table: np.ndarray, dtype: str) -> np.ndarray:
+    """Row-wise int4 encoding of a [rows][d] table: returns [rows][int4_row_bytes(d)] uint8."""
+    bits = _table_bits(table, dtype)
+    R, d = bits.shape
+    out = np.zeros((R, int4_row_bytes(d)), dtype=np.uint8)
+    _check(_load().oracle_quantize_int4(R, d, _DTYPE_CODES[dtype], _ptr(bits), _ptr(out)), "quantize_int4")
+    return out
+
+
+def emb_bag_fwd(tables, dtype: str, offsets, indices, B: int, d: int = None):
+    """Sum-pooled lookups: returns (pooled [B][T][d], magnitude) in fp64.
+    int4 tables (rows of bytes) need ``d``."""
     held, arr, rows = _tables_arg(tables, dtype)
-    T, d = len(held), held[0].shape[1]
+    T = len(held)
+    if d is None:
+        d = held[0].shape[1]
     offsets, indices = _i64(offsets), _i64(indices)
     pooled = np.empty((B, T, d), dtype=np.float64)
     mag = np.empty_like(pooled)

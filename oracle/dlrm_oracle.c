@@ -40,7 +40,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_INT4 = 3 };
 enum {
     ORACLE_OK = 0,
     ORACLE_INVALID_ARG = -1,
@@ -74,13 +74,60 @@ static double decode_bfloat16(uint16_t h)
     return (double)f;
 }
 
-static double table_element(const void *table, int dtype, int64_t pos)
+/*
+ * Row-wise 4-bit tables.  The factlen.com page ("...Force Meta's DLRM to Split
+ * Training", section "The limits of scale") reports 4-bit integer
+ * quantization of the vectors without a format; the reading here is the
+ * common row-wise affine codec: each row stores d 4-bit codes q (element 2j
+ * in the low nibble of byte j, element 2j+1 in the high nibble), then its
+ * fp32 scale s and fp32 bias b; the row is padded to a multiple of 16 bytes.
+ * An element's value is b + s q.
+ */
+static int64_t int4_row_bytes(int d)
+{
+    return ((int64_t)d / 2 + 8 + 15) / 16 * 16;
+}
+
+static void int4_params(const void *table, int d, int64_t r, float *scale, float *bias)
+{
+    const uint8_t *row = (const uint8_t *)table + r * int4_row_bytes(d);
+    memcpy(scale, row + d / 2, 4);
+    memcpy(bias, row + d / 2 + 4, 4);
+}
+
+static int int4_code(const void *table, int d, int64_t r, int e)
+{
+    const uint8_t *row = (const uint8_t *)table + r * int4_row_bytes(d);
+    return (row[e / 2] >> (4 * (e & 1))) & 15;
+}
+
+/* Element pos = r * d + e of a table; int4 tables need d to find the row. */
+static double table_element(const void *table, int dtype, int d, int64_t pos)
 {
     if (dtype == ORACLE_F32)
         return (double)((const float *)table)[pos];
     if (dtype == ORACLE_F16)
         return decode_binary16(((const uint16_t *)table)[pos]);
+    if (dtype == ORACLE_INT4) {
+        float s, b;
+        int64_t r = pos / d;
+        int e = (int)(pos % d);
+        int4_params(table, d, r, &s, &b);
+        return (double)b + (double)s * int4_code(table, d, r, e);
+    }
     return decode_bfloat16(((const uint16_t *)table)[pos]);
+}
+
+/* The element's magnitude: |value|, or |b| + |s q| for a decoded int4 code. */
+static double table_element_mag(const void *table, int dtype, int d, int64_t pos)
+{
+    if (dtype == ORACLE_INT4) {
+        float s, b;
+        int64_t r = pos / d;
+        int4_params(table, d, r, &s, &b);
+        return fabs((double)b) + fabs((double)s * int4_code(table, d, r, (int)(pos % d)));
+    }
+    return fabs(table_element(table, dtype, d, pos));
 }
 
 static double mag_or_abs(const double *mag, const double *val, int64_t i)
@@ -94,7 +141,7 @@ int oracle_decode(int dtype, const void *src, int64_t n, double *dst)
     if (dtype < ORACLE_F32 || dtype > ORACLE_BF16 || n < 0)
         return ORACLE_INVALID_ARG;
     for (int64_t i = 0; i < n; i++)
-        dst[i] = table_element(src, dtype, i);
+        dst[i] = table_element(src, dtype, 1, i);
     return ORACLE_OK;
 }
 
@@ -123,7 +170,8 @@ int oracle_emb_bag_fwd(int T, int d, int dtype, const void *const *tables, const
                        int64_t B, const int64_t *offsets, const int64_t *indices, int64_t nnz,
                        double *pooled, double *pooled_mag)
 {
-    if (T <= 0 || d <= 0 || B < 0 || dtype < ORACLE_F32 || dtype > ORACLE_BF16)
+    if (T <= 0 || d <= 0 || B < 0 || dtype < ORACLE_F32 || dtype > ORACLE_INT4 ||
+        (dtype == ORACLE_INT4 && d % 2 != 0))
         return ORACLE_INVALID_ARG;
     int st = check_offsets(T, B, offsets, nnz);
     if (st != ORACLE_OK)
@@ -141,9 +189,8 @@ int oracle_emb_bag_fwd(int T, int d, int dtype, const void *const *tables, const
                 if (r < 0 || r >= rows[t])
                     return ORACLE_INDEX_OOB;
                 for (int e = 0; e < d; e++) {
-                    double v = table_element(tables[t], dtype, r * d + e);
-                    out[e] += v;
-                    mag[e] += fabs(v);
+                    out[e] += table_element(tables[t], dtype, d, r * d + e);
+                    mag[e] += table_element_mag(tables[t], dtype, d, r * d + e);
                 }
             }
         }
@@ -421,7 +468,7 @@ int oracle_sgd(int T, int d, int dtype, const void *const *tables, const int64_t
                 g += dpooled[i];
                 gm += mag_or_abs(dpooled_mag, dpooled, i);
             }
-            double w = table_element(tables[t], dtype, r * d + e);
+            double w = table_element(tables[t], dtype, d, r * d + e);
             grad[u * d + e] = g;
             grad_mag[u * d + e] = gm;
             new_row[u * d + e] = w - lr * g;
@@ -485,7 +532,7 @@ int oracle_adagrad(int T, int d, int dtype, const void *const *tables, const int
         new_state_mag[u] = fabs(state[u]) + qm / d;
         const double root = sqrt(s1), den = root + eps;
         for (int e = 0; e < d; e++) {
-            const double w = table_element(tables[t], dtype, r * d + e);
+            const double w = table_element(tables[t], dtype, d, r * d + e);
             if (g[e] == 0.0) {
                 new_row[u * d + e] = w;
                 new_row_mag[u * d + e] = fabs(w) + (den > 0.0 ? fabs(lr) / den * gm[e] : 0.0);
@@ -498,5 +545,55 @@ int oracle_adagrad(int T, int d, int dtype, const void *const *tables, const int
         }
     }
     return ORACLE_OK;
+}
+
+/*
+ * Encodes a table of R rows of d values (fp32, fp16 or bf16; d even) into
+ * the row-wise int4 layout above.  Per row, in fp32 arithmetic (the codes
+ * are integers decided by floating point, so they are decided in one stated
+ * precision): lo and hi are the row's minimum and maximum, s = (hi - lo) / 15,
+ * b = lo (a zero minimum stored as +0), and q = the nearest integer (ties to
+ * even) to (w - lo) / s, kept in 0 .. 15; a constant row (s = 0) gets q = 0.
+ * Padding bytes are zero.  Rows are expected to be finite.
+ */
+int oracle_quantize_int4(int64_t R, int d, int src_dtype, const void *src, uint8_t *dst)
+{
+    if (R < 0 || d <= 0 || d % 2 != 0 || src_dtype < ORACLE_F32 || src_dtype > ORACLE_BF16)
+        return ORACLE_INVALID_ARG;
+    const int64_t rb = int4_row_bytes(d);
+    for (int64_t r = 0; r < R; r++) {
+        uint8_t *row = dst + r * rb;
+        memset(row, 0, (size_t)rb);
+        float lo = (float)table_element(src, src_dtype, d, r * d), hi = lo;
+        for (int e = 1; e < d; e++) {
+            float w = (float)table_element(src, src_dtype, d, r * d + e);
+            if (w < lo)
+                lo = w;
+            if (w > hi)
+                hi = w;
+        }
+        lo = lo + 0.0f; /* -0 becomes +0, so that the stored bias is unique */
+        float range = hi - lo;
+        float scale = range / 15.0f;
+        for (int e = 0; e < d; e++) {
+            int q = 0;
+            if (scale > 0.0f) {
+                float w = (float)table_element(src, src_dtype, d, r * d + e);
+                float diff = w - lo;
+                float x = diff / scale;
+                q = (int)rintf(x);
+                q = q < 0 ? 0 : (q > 15 ? 15 : q);
+            }
+            row[e / 2] |= (uint8_t)(q << (4 * (e & 1)));
+        }
+        memcpy(row + d / 2, &scale, 4);
+        memcpy(row + d / 2 + 4, &lo, 4);
+    }
+    return ORACLE_OK;
+}
+
+int64_t oracle_int4_row_bytes(int d)
+{
+    return int4_row_bytes(d);
 }
 

@@ -518,3 +518,84 @@ def test_alongside_backward_by_finite_differences(inc):
             m[idx] -= h
             fd = ((loss(p, emb) - loss(m, emb)) if which == 0 else (loss(e0, p) - loss(e0, m))) / (2 * h)
             assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd))
+
+
+# ------------------------------------------------------ row-wise int4 codec ---
+
+def _unpack_int4(qt, d):
+    """Independent numpy decode of an int4 table: codes, scales, biases."""
+    qt = np.asarray(qt, dtype=np.uint8)
+    codes = np.empty((qt.shape[0], d), dtype=np.int64)
+    codes[:, 0::2] = qt[:, :d // 2] & 15
+    codes[:, 1::2] = qt[:, :d // 2] >> 4
+    s = qt[:, d // 2:d // 2 + 4].copy().view(np.float32)[:, 0].astype(np.float64)
+    b = qt[:, d // 2 + 4:d // 2 + 8].copy().view(np.float32)[:, 0].astype(np.float64)
+    return codes, s, b
+
+
+def test_int4_worked_example():
+    g = _golden.load("int4_worked_example.txt")
+    q = oracle.quantize_int4(g["row"].reshape(1, 4).astype(np.float32), "f32")
+    np.testing.assert_array_equal(q[0], g["bytes"].astype(np.uint8))
+    pooled, _ = oracle.emb_bag_fwd([q], "int4", np.array([0, 1]), np.array([0]), 1, d=4)
+    np.testing.assert_array_equal(pooled[0, 0], g["decoded"])
+
+
+def test_int4_values_on_the_grid_round_trip_exactly():
+    # rows lo + k s with s a power of two and k = 0..15 (both ends present)
+    rng = np.random.default_rng(31)
+    d, R = 24, 40
+    lo = rng.integers(-64, 64, R).astype(np.float64) / 8
+    s = 2.0 ** rng.integers(-6, 2, R).astype(np.float64)
+    k = rng.integers(0, 16, (R, d))
+    k[:, 0], k[:, 1] = 0, 15
+    w = (lo[:, None] + s[:, None] * k).astype(np.float32)
+    q = oracle.quantize_int4(w, "f32")
+    codes, sc, bi = _unpack_int4(q, d)
+    np.testing.assert_array_equal(codes, k)
+    np.testing.assert_array_equal(sc, s)
+    np.testing.assert_array_equal(bi, lo)
+    assert oracle.int4_row_bytes(d) == 32 and q.shape == (R, 32) and not q[:, 20:].any()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_int4_error_is_at_most_half_a_step(dtype):
+    rng = np.random.default_rng(32)
+    w = rng.standard_normal((50, 64)).astype(np.float32)
+    if dtype == "f16":
+        w = w.astype(np.float16)
+    elif dtype == "bf16":
+        w = W.f32_to_bf16_bits(w)
+    q = oracle.quantize_int4(w, dtype)
+    codes, s, b = _unpack_int4(q, 64)
+    vals = oracle.decode(w, dtype)
+    np.testing.assert_array_equal(b, vals.min(axis=1).astype(np.float32))
+    assert np.all(codes >= 0) and np.all(codes <= 15)
+    err = np.abs(b[:, None] + s[:, None] * codes - vals)
+    assert np.all(err <= s[:, None] * (0.5 + 1e-5))
+
+
+def test_int4_constant_row_and_signed_zero():
+    w = np.zeros((3, 8), dtype=np.float32)
+    w[0] = 2.5
+    w[1] = -0.0
+    w[2, ::2] = -0.0  # a mix of -0 and +0 is a constant row too
+    q = oracle.quantize_int4(w, "f32")
+    codes, s, b = _unpack_int4(q, 8)
+    assert np.all(codes == 0) and np.all(s == 0)
+    np.testing.assert_array_equal(b, [2.5, 0.0, 0.0])
+    assert not np.signbit(q[1, 8:12].copy().view(np.float32))[0]  # the stored bias is +0
+
+
+def test_int4_pooling_sums_the_decoded_rows():
+    rng = np.random.default_rng(33)
+    rows, T, B, d = [13, 6], 2, 9, 16
+    tables = [oracle.quantize_int4(rng.standard_normal((r, d)).astype(np.float32), "f32") for r in rows]
+    offsets, indices = _csr(_random_bags(rng, T, B, rows, 5))
+    pooled, _ = oracle.emb_bag_fwd(tables, "int4", offsets, indices, B, d=d)
+    for t in range(T):
+        codes, s, b = _unpack_int4(tables[t], d)
+        dec = b[:, None] + s[:, None] * codes
+        for bb in range(B):
+            lo, hi = offsets[t * B + bb], offsets[t * B + bb + 1]
+            np.testing.assert_allclose(pooled[bb, t], dec[indices[lo:hi]].sum(axis=0), rtol=1e-14, atol=1e-14)
