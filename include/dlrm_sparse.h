@@ -43,7 +43,7 @@ extern "C" {
 
 typedef void *dlrm_stream_t; /* a cudaStream_t */
 
-enum dlrm_dtype { DLRM_F32 = 0, DLRM_F16 = 1, DLRM_BF16 = 2 };
+enum dlrm_dtype { DLRM_F32 = 0, DLRM_F16 = 1, DLRM_BF16 = 2, DLRM_INT4 = 3 };
 
 enum dlrm_status {
     DLRM_OK = 0,
@@ -91,6 +91,36 @@ int dlrm_emb_bag_fwd(const void *const *tables, const int64_t *rows, int T, int 
                      const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
                      float *out, int64_t out_sample_stride, int64_t out_table_stride,
                      int32_t *err_flag, dlrm_stream_t stream);
+
+/*
+ * Row-wise int4 tables (DLRM_INT4).  The factlen.com page ("Terabyte Embedding
+ * Tables and Compute-Bound Neural Layers Force Meta's DLRM to Split
+ * Training", section "The limits of scale") reports 4-bit integer
+ * quantization of the vectors; the format here is the row-wise affine codec.
+ * A row of d values (d % 8 == 0, d <= 512) takes dlrm_int4_row_bytes(d)
+ * bytes: d codes q of 4 bits (element 2j in the low nibble of byte j, 2j+1 in
+ * the high nibble), then the row's fp32 scale s and fp32 bias b, then zero
+ * padding to a multiple of 16 bytes.  Element e of the row has the value
+ * b + s q[e].  An int4 table pointer is 16-byte aligned and holds rows[t]
+ * such rows.  dlrm_emb_bag_fwd and dlrm_emb_bag_interact_fwd (two-kernel
+ * path) read int4 tables, with the output 16-byte aligned and its strides
+ * multiples of 4 (DLRM_ERR_UNSUPPORTED otherwise); the backward calls
+ * return DLRM_ERR_UNSUPPORTED for them (4-bit tables are served, not
+ * trained).  The pooled sum is fp32: per element the sum of s q, plus the
+ * sum of the biases.
+ */
+int64_t dlrm_int4_row_bytes(int d);  /* -1 for d <= 0 or odd d */
+
+/*
+ * Encodes rows x d values (src: device, dtype DLRM_F32/F16/BF16, row stride
+ * d, element-aligned) into the int4 layout at dst (device, 16-byte aligned,
+ * rows * dlrm_int4_row_bytes(d) bytes).  Per row, in fp32: lo and hi the
+ * minimum and maximum (a zero stored as +0), s = (hi - lo) / 15, b = lo, and
+ * q = round-half-to-even((w - lo) / s) kept in 0 .. 15 (all 0 when s == 0);
+ * the subtraction and the divisions are IEEE-rounded, so the codes are
+ * reproducible bit for bit.  Rows are expected to be finite.
+ */
+int dlrm_quantize_int4(const void *src, int src_dtype, int64_t rows, int d, void *dst, dlrm_stream_t stream);
 
 /*
  * Number of interaction terms over F = N + 1 vectors (e0 and N pooled

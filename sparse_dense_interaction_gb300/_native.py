@@ -16,7 +16,7 @@ import torch
 
 from . import build as _build
 
-F32, F16, BF16 = 0, 1, 2
+F32, F16, BF16, INT4 = 0, 1, 2, 3
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL = 0, -1, -2, -3
 ERR_INDEX_OOB, ERR_BAD_OFFSETS, ERR_CAPACITY, ERR_CUDA, ERR_WAIT_TIMEOUT = -4, -5, -6, -7, -8
 FLAG_INDEX_OOB, FLAG_BAD_OFFSETS, FLAG_CAPACITY, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
@@ -60,6 +60,8 @@ SIGNATURES = {
                                         _vp]),
     "dlrm_emb_bag_reduce_adagrad": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i64, _i64, _vp, _i64, _i64, _f32,
                                            _f32, _vp, _i64, _vp, _sz, _vp, _vp]),
+    "dlrm_int4_row_bytes": (_i64, [_i32]),
+    "dlrm_quantize_int4": (_i32, [_vp, _i32, _i64, _i32, _vp, _vp]),
     "dlrm_read_error": (_i32, [_vp, _vp]),
     "dlrm_clear_error": (_i32, [_vp, _vp]),
     "dlrm_status_string": (ctypes.c_char_p, [_i32]),
@@ -118,20 +120,42 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def _tables(tables):
+def _tables(tables, d=None):
+    """Pointers, rows, T, d and type of a list of tables.  uint8 tables are
+    row-wise int4 tables ([rows][dlrm_int4_row_bytes(d)]) and need ``d``."""
     T = len(tables)
     ptrs = (ctypes.c_void_p * max(T, 1))(*[t.data_ptr() for t in tables])
     rows = (ctypes.c_int64 * max(T, 1))(*[t.shape[0] for t in tables])
-    dtype = _TORCH_DTYPES[tables[0].dtype]
     for t in tables:
         if t.dtype != tables[0].dtype or t.dim() != 2 or t.stride(1) != 1 or t.stride(0) != t.shape[1]:
             raise ValueError("tables must share one dtype and be contiguous [rows][d]")
-    return ptrs, rows, T, tables[0].shape[1], dtype
+    if tables[0].dtype == torch.uint8:
+        if d is None or tables[0].shape[1] != dlrm_int4_row_bytes(d):
+            raise ValueError("int4 tables need d, with rows of dlrm_int4_row_bytes(d) bytes")
+        return ptrs, rows, T, d, INT4
+    return ptrs, rows, T, tables[0].shape[1], _TORCH_DTYPES[tables[0].dtype]
 
 
-def dlrm_emb_bag_fwd(tables, offsets, indices, B: int, out, err_flag=None, stream=None):
-    """Sum-pooled lookups into ``out`` ([B][T][d] fp32, any strides, last dim 1)."""
-    ptrs, rows, T, d, dtype = _tables(tables)
+def dlrm_int4_row_bytes(d: int) -> int:
+    return int(load().dlrm_int4_row_bytes(d))
+
+
+def dlrm_quantize_int4(src, stream=None):
+    """Row-wise int4 encoding of a [rows][d] fp32/fp16/bf16 CUDA table:
+    returns a uint8 [rows][dlrm_int4_row_bytes(d)] tensor."""
+    if src.dim() != 2 or src.stride(1) != 1 or src.stride(0) != src.shape[1]:
+        raise ValueError("src must be a contiguous [rows][d] table")
+    R, d = src.shape
+    dst = torch.empty((R, max(dlrm_int4_row_bytes(d), 0)), dtype=torch.uint8, device=src.device)
+    _check(load().dlrm_quantize_int4(src.data_ptr(), _TORCH_DTYPES[src.dtype], R, d, dst.data_ptr(),
+                                     _stream(stream)), "dlrm_quantize_int4")
+    return dst
+
+
+def dlrm_emb_bag_fwd(tables, offsets, indices, B: int, out, err_flag=None, stream=None, d=None):
+    """Sum-pooled lookups into ``out`` ([B][T][d] fp32, any strides, last dim 1).
+    ``d`` is needed only for int4 (uint8) tables."""
+    ptrs, rows, T, d, dtype = _tables(tables, d)
     if out.stride(2) != 1:
         raise ValueError("out must have unit stride in its last dimension")
     _check(load().dlrm_emb_bag_fwd(ptrs, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices),
@@ -252,12 +276,12 @@ def dlrm_emb_bag_reduce_sgd(tables, nnz: int, B: int, dpooled, lr: float, worksp
 
 
 def dlrm_emb_bag_interact_fwd(tables, offsets, indices, B: int, e0, include_self: bool, y, pooled=None,
-                              err_flag=None, stream=None, alongside: bool = False):
+                              err_flag=None, stream=None, alongside: bool = False, d=None):
     """Lookup + interaction forward in one call: ``y`` ([B][d + P] fp32, last
     dim 1) receives what :func:`dlrm_interact_fwd` would give on the pooled
     vectors of :func:`dlrm_emb_bag_fwd`; ``pooled`` ([B][T][d] fp32, optional)
     also receives those pooled vectors."""
-    ptrs, rows, T, d, dtype = _tables(tables)
+    ptrs, rows, T, d, dtype = _tables(tables, d)
     if e0.stride(1) != 1 or y.stride(1) != 1:
         raise ValueError("e0 and y must have unit stride in their last dimension")
     pss = pts = 0

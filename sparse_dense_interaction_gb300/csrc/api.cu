@@ -35,6 +35,10 @@ int sm_count()
 
 // kernels (defined in the other translation units)
 bool emb_bag_fwd_vectorisable(const TableSet &, int, int, int, const float *, int64_t, int64_t);
+int64_t int4_row_bytes(int);
+int launch_emb_bag_fwd_int4(const TableSet &, int, int, const int64_t *, const int64_t *, int64_t, int64_t, float *,
+                            int64_t, int64_t, int32_t *, cudaStream_t);
+int launch_quantize_int4(const void *, int, int64_t, int, void *, cudaStream_t);
 int launch_emb_bag_fwd(const TableSet &, int, int, int, bool, const int64_t *, const int64_t *, int64_t,
                        int64_t, float *, int64_t, int64_t, int32_t *, cudaStream_t);
 int launch_interact_fwd(const float *, int64_t, const float *, int64_t, int, int, int64_t, int, float *,
@@ -63,7 +67,9 @@ int launch_reduce_sgd(const TableSet &, int, int, int, int64_t, int64_t, const f
 // leaves headroom for tile and chunk arithmetic.
 static const int64_t kMaxLookups = (int64_t)1 << 31;
 
-static int elem_bytes(int dtype) { return dtype == DLRM_F32 ? 4 : 2; }
+static int elem_bytes(int dtype) { return dtype == DLRM_F32 ? 4 : 2; }  // of the float table types
+
+static const int kInt4MaxD = 512;  // 32 lanes of 16 codes
 
 static bool aligned(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
@@ -73,9 +79,11 @@ static int make_tables(const void *const *tables, const int64_t *rows, int T, in
 {
     if (!tables || !rows || T <= 0 || d <= 0)
         return DLRM_ERR_INVALID_ARG;
-    if (dtype != DLRM_F32 && dtype != DLRM_F16 && dtype != DLRM_BF16)
+    if (dtype != DLRM_F32 && dtype != DLRM_F16 && dtype != DLRM_BF16 && dtype != DLRM_INT4)
         return DLRM_ERR_INVALID_ARG;
-    if (T > DLRM_MAX_TABLES)
+    if (dtype == DLRM_INT4 && d % 2 != 0)
+        return DLRM_ERR_INVALID_ARG;
+    if (T > DLRM_MAX_TABLES || (dtype == DLRM_INT4 && (d % 8 != 0 || d > kInt4MaxD)))
         return DLRM_ERR_UNSUPPORTED;
     std::memset(&ts, 0, sizeof ts);
     for (int t = 0; t < T; t++) {
@@ -83,12 +91,25 @@ static int make_tables(const void *const *tables, const int64_t *rows, int T, in
             return DLRM_ERR_INVALID_ARG;
         if (rows[t] > (int64_t)0xfffffffeLL)
             return DLRM_ERR_UNSUPPORTED;
-        if (!aligned(tables[t], (size_t)elem_bytes(dtype)))
+        if (!aligned(tables[t], dtype == DLRM_INT4 ? 16 : (size_t)elem_bytes(dtype)))
             return DLRM_ERR_INVALID_ARG;
         ts.ptr[t] = tables[t];
         ts.rows[t] = rows[t];
     }
     return DLRM_OK;
+}
+
+// The pooled lookup into out, for every table type.
+static int launch_lookup(const TableSet &ts, int T, int d, int dtype, const int64_t *offsets, const int64_t *indices,
+                         int64_t nnz, int64_t B, float *out, int64_t oss, int64_t ots, int32_t *err, cudaStream_t st)
+{
+    if (dtype == DLRM_INT4) {
+        if (!aligned(out, 16) || oss % 4 != 0 || ots % 4 != 0)
+            return DLRM_ERR_UNSUPPORTED;
+        return launch_emb_bag_fwd_int4(ts, T, d, offsets, indices, nnz, B, out, oss, ots, err, st);
+    }
+    const bool vec = emb_bag_fwd_vectorisable(ts, T, d, elem_bytes(dtype), out, oss, ots);
+    return launch_emb_bag_fwd(ts, T, d, dtype, vec, offsets, indices, nnz, B, out, oss, ots, err, st);
 }
 
 }  // namespace dlrm
@@ -114,10 +135,30 @@ int dlrm_emb_bag_fwd(const void *const *tables, const int64_t *rows, int T, int 
         return DLRM_ERR_INVALID_ARG;
     if (!aligned(offsets, 8) || (indices && !aligned(indices, 8)))
         return DLRM_ERR_INVALID_ARG;
-    const bool vec = emb_bag_fwd_vectorisable(ts, T, d, elem_bytes(dtype), out, out_sample_stride,
-                                              out_table_stride);
-    return launch_emb_bag_fwd(ts, T, d, dtype, vec, offsets, indices, nnz, B, out, out_sample_stride,
-                              out_table_stride, err_flag, static_cast<cudaStream_t>(stream));
+    return launch_lookup(ts, T, d, dtype, offsets, indices, nnz, B, out, out_sample_stride, out_table_stride,
+                         err_flag, static_cast<cudaStream_t>(stream));
+}
+
+int64_t dlrm_int4_row_bytes(int d)
+{
+    if (d <= 0 || d % 2 != 0)
+        return -1;
+    return int4_row_bytes(d);
+}
+
+int dlrm_quantize_int4(const void *src, int src_dtype, int64_t rows, int d, void *dst, dlrm_stream_t stream)
+{
+    if (rows < 0 || d <= 0 || d % 2 != 0)
+        return DLRM_ERR_INVALID_ARG;
+    if (src_dtype != DLRM_F32 && src_dtype != DLRM_F16 && src_dtype != DLRM_BF16)
+        return DLRM_ERR_INVALID_ARG;
+    if (d % 8 != 0 || d > kInt4MaxD)
+        return DLRM_ERR_UNSUPPORTED;
+    if (rows == 0)
+        return DLRM_OK;
+    if (!src || !dst || !aligned(src, (size_t)elem_bytes(src_dtype)) || !aligned(dst, 16))
+        return DLRM_ERR_INVALID_ARG;
+    return launch_quantize_int4(src, src_dtype, rows, d, dst, static_cast<cudaStream_t>(stream));
 }
 
 int64_t dlrm_num_pairs(int N, int include_self)
@@ -215,7 +256,7 @@ int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, in
         return DLRM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t row_bytes = (int64_t)d * elem_bytes(dtype);
-    bool fused = row_bytes % 16 == 0 && row_bytes <= 1024;
+    bool fused = dtype != DLRM_INT4 && row_bytes % 16 == 0 && row_bytes <= 1024;
     for (int t = 0; t < T && fused; t++)
         fused = aligned(tables[t], 16);
     if (pooled)
@@ -228,10 +269,8 @@ int dlrm_emb_bag_interact_fwd(const void *const *tables, const int64_t *rows, in
     // the two calls it fuses, through the caller's pooled block
     if (!pooled || pooled_table_stride != d)
         return DLRM_ERR_UNSUPPORTED;
-    const bool vec = emb_bag_fwd_vectorisable(ts, T, d, elem_bytes(dtype), pooled, pooled_sample_stride,
-                                              pooled_table_stride);
-    s = launch_emb_bag_fwd(ts, T, d, dtype, vec, offsets, indices, nnz, B, pooled, pooled_sample_stride,
-                           pooled_table_stride, err_flag, st);
+    s = launch_lookup(ts, T, d, dtype, offsets, indices, nnz, B, pooled, pooled_sample_stride,
+                      pooled_table_stride, err_flag, st);
     if (s != DLRM_OK)
         return s;
     return launch_interact_fwd(e0, e0_stride, pooled, pooled_sample_stride, T, d, B, mode, y, y_stride, st);
@@ -291,6 +330,8 @@ int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d,
     int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
     if (s != DLRM_OK)
         return s;
+    if (dtype == DLRM_INT4)  // 4-bit tables are looked up, not trained
+        return DLRM_ERR_UNSUPPORTED;
     if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=
         DLRM_OK)
         return s;
@@ -335,6 +376,8 @@ int dlrm_emb_bag_reduce_sgd(void *const *tables, const int64_t *rows, int T, int
     int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
     if (s != DLRM_OK)
         return s;
+    if (dtype == DLRM_INT4)  // 4-bit tables are looked up, not trained
+        return DLRM_ERR_UNSUPPORTED;
     if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=
         DLRM_OK)
         return s;
@@ -377,6 +420,8 @@ int dlrm_emb_bag_bwd_adagrad(void *const *tables, float *const *state, const int
     int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
     if (s != DLRM_OK)
         return s;
+    if (dtype == DLRM_INT4)  // 4-bit tables are looked up, not trained
+        return DLRM_ERR_UNSUPPORTED;
     if ((s = check_adagrad(state, T, d, lr, eps)) != DLRM_OK)
         return s;
     if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=
@@ -402,6 +447,8 @@ int dlrm_emb_bag_reduce_adagrad(void *const *tables, float *const *state, const 
     int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
     if (s != DLRM_OK)
         return s;
+    if (dtype == DLRM_INT4)  // 4-bit tables are looked up, not trained
+        return DLRM_ERR_UNSUPPORTED;
     if ((s = check_adagrad(state, T, d, lr, eps)) != DLRM_OK)
         return s;
     if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=

@@ -74,7 +74,11 @@ def test_forward_rejects_bad_arguments(lib):
         kw.get("offsets", FAKE), FAKE, 10, kw.get("B", 2), kw.get("out", FAKE), 64, 16, None, None)
     assert call(T=0) == _native.ERR_INVALID_ARG
     assert call(d=0) == _native.ERR_INVALID_ARG
-    assert call(dtype=3) == _native.ERR_INVALID_ARG
+    assert call(dtype=4) == _native.ERR_INVALID_ARG  # no such table type
+    # int4 tables: d must be even (else invalid), a multiple of 8 and at most 512
+    assert call(dtype=_native.INT4, d=13) == _native.ERR_INVALID_ARG
+    assert call(dtype=_native.INT4, d=12) == _native.ERR_UNSUPPORTED
+    assert call(dtype=_native.INT4, d=520) == _native.ERR_UNSUPPORTED
     assert call(tables=None) == _native.ERR_INVALID_ARG
     assert call(offsets=None) == _native.ERR_INVALID_ARG
     assert call(out=None) == _native.ERR_INVALID_ARG
@@ -126,6 +130,23 @@ def test_fused_forward_rejects_bad_arguments(lib):
     big_p, big_r = _tables(128)
     assert call(tables=big_p, rows=big_r, T=128, ys=100000) == _native.ERR_UNSUPPORTED  # N <= 127
     assert call(B=0) == _native.OK
+    assert lib.dlrm_kernel_launch_count() == 0
+
+
+def test_int4_calls_reject_bad_arguments(lib):
+    assert lib.dlrm_int4_row_bytes(128) == 80 and lib.dlrm_int4_row_bytes(40) == 32
+    assert lib.dlrm_int4_row_bytes(7) == -1 and lib.dlrm_int4_row_bytes(0) == -1
+    q = lambda src_dtype=0, rows=4, d=16, dst=FAKE: lib.dlrm_quantize_int4(FAKE, src_dtype, rows, d, dst, None)
+    assert q(src_dtype=3) == _native.ERR_INVALID_ARG  # int4 is not a source type
+    assert q(d=15) == _native.ERR_INVALID_ARG
+    assert q(d=20) == _native.ERR_UNSUPPORTED  # even, not a multiple of 8
+    assert q(dst=FAKE + 8) == _native.ERR_INVALID_ARG  # the encoded rows start 16-byte aligned
+    assert q(rows=0) == _native.OK
+    # 4-bit tables are not trained
+    p, r = _tables(2)
+    need = sdi.dlrm_emb_bag_bwd_workspace_size(2, 8, 100, 16)
+    assert lib.dlrm_emb_bag_bwd_sgd(p, r, 2, 16, _native.INT4, FAKE, FAKE, 100, 8, FAKE, 32, 16, 0.1, None, 0,
+                                    0x100000, need, None, None, None) == _native.ERR_UNSUPPORTED
     assert lib.dlrm_kernel_launch_count() == 0
 
 
