@@ -572,7 +572,8 @@ int oracle_quantize_int4(int64_t R, int d, int src_dtype, const void *src, uint8
             if (w > hi)
                 hi = w;
         }
-        lo = lo + 0.0f; /* -0 becomes +0, so that the stored bias is unique */
+        lo = lo + 0.0f; /* -0 becomes +0, so that the stored bias and scale are unique */
+        hi = hi + 0.0f;
         float range = hi - lo;
         float scale = range / 15.0f;
         for (int e = 0; e < d; e++) {
