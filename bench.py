@@ -304,7 +304,7 @@ class Step:
         self.schedule, self.fwd, self.optimizer = schedule, fwd, optimizer
         self.state = ([torch.zeros(r, dtype=torch.float32, device=dev) for r in cfg["rows"]]
                       if optimizer == "adagrad" else None)
-        self.side = torch.cuda.Stream(dev)
+        self.side = torch.cuda.Stream(dev, priority=-1)  # its small sort kernels go first when SMs free up
         self.coalesced = torch.cuda.Event()
 
     def run(self, prof=None):

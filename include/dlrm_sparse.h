@@ -343,7 +343,7 @@ int dlrm_emb_bag_reduce_adagrad(void *const *tables, float *const *state, const 
  * DLRM_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library holds until the process exits.
  *  - Sizes whose scratch would not fit (dlrm_emb_bag_bwd_workspace_size(T, B,
- *    nnz, d) > DLRM_NOALLOC_SCRATCH_BYTES; about 1.8M lookups at d = 128) are
+ *    nnz, d) > DLRM_NOALLOC_SCRATCH_BYTES; about 1.7M lookups at d = 128) are
  *    refused with DLRM_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  *  - The first call on each device looks up the array's device address (a
  *    CUDA runtime query, made with that device current); make that first call
