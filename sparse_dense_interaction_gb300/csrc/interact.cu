@@ -42,6 +42,10 @@ __device__ __forceinline__ void load8(const float *src, int k, int d, bool vec, 
     }
 }
 
+// TS: staged row of Zt, Fp columns rounded up to a multiple of 32 (32, 64 or
+// 128); a compile-time row width makes every shared-memory address of the
+// inner loops an immediate offset.
+template <int TS>
 __global__ void __launch_bounds__(1024)
 interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__restrict__ emb,
                     int64_t embs, int N, int d, int64_t B, int mode, float *__restrict__ y,
@@ -53,7 +57,6 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
     const int F = N + 1;
     const int64_t poff = along ? (int64_t)F * d : d;  // first pair column
     const int Fp = (F + 3) & ~3;
-    const int TS = (Fp + 31) & ~31;                     // staged row: Fp columns, swizzled
     const int nTR = Fp / 4;
     const int ntiles = nTR * (nTR + 1) / 2;
     const int64_t P = inc ? (int64_t)F * (F + 1) / 2 : (int64_t)F * (F - 1) / 2;
@@ -78,17 +81,30 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
 
     const bool vec_y = vec_out != 0;
     const int rblocks = (F + 7) / 8;
+    // staging work items: (sample, block of 8 rows) per warp, stepped by the
+    // warp count without dividing in the loop
+    const int lane = tid & 31, nwarps = blockDim.x >> 5;
+    const int items = S * rblocks;
+    const int wi0 = tid >> 5;
+    const int ss0 = wi0 / rblocks, ib0 = wi0 - ss0 * rblocks;
+    const int dss = nwarps / rblocks, dib = nwarps - dss * rblocks;
+    const int q = lane >> 3;  // column octet of the lane
     for (int kc = 0; kc < d; kc += kKC) {
         // stage: a warp reads 8 rows x 4 column octets (32 bytes per lane, so
         // each row chunk is one coalesced 128-byte read) and transposes them
-        for (int li = tid; li < S * rblocks * 32; li += blockDim.x) {
-            const int lane = li & 31;
-            const int i = ((li >> 5) % rblocks) * 8 + (lane & 7);
-            const int q = lane >> 3;
-            const int ss = (li >> 5) / rblocks;
+        int ss = ss0, ib = ib0;
+        for (int wi = wi0; wi < items; wi += nwarps) {
+            const int i = ib * 8 + (lane & 7);
+            const int cur_ss = ss;
+            ss += dss;
+            ib += dib;
+            if (ib >= rblocks) {
+                ib -= rblocks;
+                ss++;
+            }
             if (i >= F)
                 continue;
-            const int64_t b = b0 + ss;
+            const int64_t b = b0 + cur_ss;
             const int k = kc + 8 * q;
             float v[8];
             if (b < B && k < d) {
@@ -108,29 +124,35 @@ interact_fwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
             } else {
 #pragma unroll
                 for (int m = 0; m < 8; m++)
-                    v[m] = 0.f;
+                    v[m] = 0.f;  // rows past d (or past B) are zero: the inner loop runs whole chunks
             }
-            float *zt = Zt + (size_t)ss * kKC * TS;
+            // the 8 rows of an octet share one swizzle: (8q + m) >> 3 == q
+            float *zt = Zt + (size_t)cur_ss * kKC * TS + 8 * q * TS + zt_col(8 * q, i);
 #pragma unroll
             for (int m = 0; m < 8; m++)
-                zt[(8 * q + m) * TS + zt_col(8 * q + m, i)] = v[m];
+                zt[m * TS] = v[m];
         }
         __syncthreads();
         if (active) {
             const int I = tileI[tile], J = tileJ[tile];
             const float *zs = Zt + (size_t)s * kKC * TS;
-            const int kn = min(kKC, d - kc);
-#pragma unroll 4
-            for (int k = 0; k < kn; k++) {
-                const float4 a = *reinterpret_cast<const float4 *>(zs + (size_t)k * TS + zt_col(k, 4 * I));
-                const float4 bb = *reinterpret_cast<const float4 *>(zs + (size_t)k * TS + zt_col(k, 4 * J));
-                const float av[4] = {a.x, a.y, a.z, a.w};
-                const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
-                for (int r = 0; r < 4; r++)
+            for (int kb = 0; kb < kKC / 8; kb++) {
+                // within 8 consecutive rows the swizzle of a column group is fixed
+                const float *pa = zs + kb * 8 * TS + ((I ^ (kb << 1)) << 2);
+                const float *pb = zs + kb * 8 * TS + ((J ^ (kb << 1)) << 2);
 #pragma unroll
-                    for (int c = 0; c < 4; c++)
-                        acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+                for (int m = 0; m < 8; m++) {
+                    const float4 a = *reinterpret_cast<const float4 *>(pa + m * TS);
+                    const float4 bb = *reinterpret_cast<const float4 *>(pb + m * TS);
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+                    const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                    for (int r = 0; r < 4; r++)
+#pragma unroll
+                        for (int c = 0; c < 4; c++)
+                            acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+                }
             }
         }
         __syncthreads();
@@ -282,9 +304,16 @@ interact_bwd_kernel(const float *__restrict__ e0, int64_t e0s, const float *__re
 
 static bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
+int launch_interact_fwd_tma(const float *, int64_t, const float *, int64_t, int, int, int64_t, int, float *,
+                            int64_t, cudaStream_t);
+
 int launch_interact_fwd(const float *e0, int64_t e0s, const float *emb, int64_t embs, int N, int d,
                         int64_t B, int mode, float *y, int64_t ys, cudaStream_t st)
 {
+    // the bulk-tensor-copy kernel when the copy engine can describe the operands
+    const int r = launch_interact_fwd_tma(e0, e0s, emb, embs, N, d, B, mode, y, ys, st);
+    if (r != 1)
+        return r;
     const int inc = mode & kInteractSelf;
     const int F = N + 1;
     const int Fp = (F + 3) & ~3;
@@ -300,16 +329,17 @@ int launch_interact_fwd(const float *e0, int64_t e0s, const float *emb, int64_t 
         S = (int)B;
     const int threads = ((S * ntiles + 31) / 32) * 32;
     const size_t smem = (size_t)S * per_sample + 2 * (size_t)ntiles;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(interact_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr_set = true;
-    }
     const int vec_in = d % 4 == 0 && aligned16(e0) && aligned16(emb) && e0s % 4 == 0 && embs % 4 == 0;
     const int vec_out = aligned16(y) && ys % 4 == 0;
     const int64_t grid = (B + S - 1) / S;
-    interact_fwd_kernel<<<(unsigned)grid, threads, smem, st>>>(e0, e0s, emb, embs, N, d, B, mode, y, ys,
-                                                               S, vec_in, vec_out);
+    auto kernel = TS == 32 ? interact_fwd_kernel<32> : (TS == 64 ? interact_fwd_kernel<64> : interact_fwd_kernel<128>);
+    static bool attr_set[3] = {false, false, false};
+    const int which = TS == 32 ? 0 : (TS == 64 ? 1 : 2);
+    if (!attr_set[which]) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        attr_set[which] = true;
+    }
+    kernel<<<(unsigned)grid, threads, smem, st>>>(e0, e0s, emb, embs, N, d, B, mode, y, ys, S, vec_in, vec_out);
     count_launch(st);
     return launch_status();
 }
