@@ -34,6 +34,7 @@ namespace dlrm {
 namespace {
 
 constexpr int kSpinLimitTma = 1 << 22;  // polls of a stage barrier (far beyond any copy's latency)
+constexpr int kTmaLanesPerTile = 2;     // lanes sharing a 4 x 4 tile (each sums every other column group)
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -81,6 +82,7 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 
 }  // namespace
 
+template <int KS>  // lanes per tile
 __global__ void __launch_bounds__(512, 2)
 interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid_constant__ CUtensorMap map_e0,
                         int N, int d, int64_t B, int mode, float *__restrict__ y, int64_t ys, int S, int R8)
@@ -134,11 +136,11 @@ interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __gri
             issue(1);
     }
 
-    // two adjacent lanes per tile: lane ks takes the 16-byte column groups
-    // k4 = ks, ks + 2, ks + 4, ks + 6 of each chunk
-    const int s = tid / (2 * ntiles);
-    const int rem = tid - s * 2 * ntiles;
-    const int tile = rem >> 1, ks = rem & 1;
+    // KS adjacent lanes per tile: lane ks takes the 16-byte column groups
+    // k4 = ks, ks + KS, ... of each chunk
+    const int s = tid / (KS * ntiles);
+    const int rem = tid - s * KS * ntiles;
+    const int tile = rem / KS, ks = rem % KS;
     const bool active = s < nS;
     int I = 0, J = 0;
     // row words: slot offset of the row OR its swizzle (bits 4..6); the
@@ -201,8 +203,8 @@ interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __gri
         if (active) {
             const unsigned char *sl = stg + (size_t)s * slot;
 #pragma unroll
-            for (int h = 0; h < kKC / 8; h++) {
-                const uint32_t kx = (uint32_t)(2 * h + ks) << 4;
+            for (int h = 0; h < kKC / 4 / KS; h++) {
+                const uint32_t kx = (uint32_t)(KS * h + ks) << 4;
                 float4 bv[4];
 #pragma unroll
                 for (int q = 0; q < 4; q++)
@@ -226,12 +228,14 @@ interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __gri
             issue(c + 2);
         }
     }
-    // the two lanes of a tile add their halves (all lanes of the warp take part)
+    // the lanes of a tile add their parts (all lanes of the warp take part)
 #pragma unroll
-    for (int r = 0; r < 4; r++)
+    for (int o = 1; o < KS; o <<= 1)
 #pragma unroll
-        for (int cc = 0; cc < 4; cc++)
-            acc[r][cc] += __shfl_xor_sync(0xffffffffu, acc[r][cc], 1);
+        for (int r = 0; r < 4; r++)
+#pragma unroll
+            for (int cc = 0; cc < 4; cc++)
+                acc[r][cc] += __shfl_xor_sync(0xffffffffu, acc[r][cc], o);
 
     if (failed) {
         // copies still in flight target this CTA's shared memory: wait for
@@ -250,8 +254,8 @@ interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __gri
 #pragma unroll
         for (int r = 0; r < 4; r++) {
             const int i = 4 * I + r;
-            if ((r & 1) != ks)
-                continue;  // lane ks writes rows r with r % 2 == ks
+            if (r % KS != ks)
+                continue;  // lane ks writes rows r with r % KS == ks
 #pragma unroll
             for (int cc = 0; cc < 4; cc++) {
                 const int j = 4 * J + cc;
@@ -324,7 +328,8 @@ int launch_interact_fwd_tma(const float *e0, int64_t e0s, const float *emb, int6
     auto smem_for = [&](int S) {
         return 1024 + 2 * (size_t)S * slot + ((size_t)S * P + 1) * 4 + 16 + 2 * (size_t)ntiles;
     };
-    int S = 2 * ntiles >= 512 ? 1 : 512 / (2 * ntiles);  // two lanes per tile
+    constexpr int KS = kTmaLanesPerTile;
+    int S = KS * ntiles >= 512 ? 1 : 512 / (KS * ntiles);
     if (S > 8)
         S = 8;
     while (S > 1 && smem_for(S) > 112 * 1024)
@@ -332,16 +337,16 @@ int launch_interact_fwd_tma(const float *e0, int64_t e0s, const float *emb, int6
     if (S > B)
         S = (int)B;
     const size_t smem = smem_for(S);
-    if (smem > 112 * 1024 || (int64_t)S * 2 * ntiles > 512)  // two CTAs of up to 512 threads per SM
+    if (smem > 112 * 1024 || (int64_t)S * KS * ntiles > 512)  // two CTAs of up to 512 threads per SM
         return 1;
-    const int threads = ((S * 2 * ntiles + 31) / 32) * 32;
+    const int threads = ((S * KS * ntiles + 31) / 32) * 32;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaFuncSetAttribute(interact_fwd_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        cudaFuncSetAttribute(interact_fwd_tma_kernel<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         attr_set = true;
     }
     const int64_t grid = (B + S - 1) / S;
-    interact_fwd_tma_kernel<<<(unsigned)grid, threads, smem, st>>>(map_emb, map_e0, N, d, B, mode, y, ys, S, R8);
+    interact_fwd_tma_kernel<KS><<<(unsigned)grid, threads, smem, st>>>(map_emb, map_e0, N, d, B, mode, y, ys, S, R8);
     count_launch(st);
     return launch_status();
 }
