@@ -187,3 +187,106 @@ def test_full_size_step_matches_oracle(name):
     off_t, idx_t = res["off_t"], res["idx_t"]
     del res
     _check_backward(cfg, tables, offsets, indices, off_t, idx_t)
+
+
+def _need(cfg, extra=0.0):
+    need = W.table_bytes(cfg) * 1.2 + 4e9 + extra
+    free, _ = torch.cuda.mem_get_info()
+    if free < need:
+        pytest.skip(f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free")
+
+
+def test_full_size_fused_forward_multi_hot():
+    cfg = W.make_config("multi-hot")
+    _need(cfg)
+    B, T, d, inc = cfg["B"], cfg["T"], cfg["d"], cfg["include_self"]
+    offsets, indices = W.make_indices(cfg)
+    tables = W.make_tables_device(cfg)
+    e0 = W.make_e0(cfg)
+    y = torch.empty((B, sdi.dlrm_interact_width(T, d, inc)), device=DEV)
+    pooled = torch.empty((B, T, d), device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sdi.dlrm_emb_bag_interact_fwd(tables, torch.from_numpy(offsets).to(DEV), torch.from_numpy(indices).to(DEV), B,
+                                  torch.from_numpy(e0).to(DEV), inc, y, pooled=pooled, err_flag=flag)
+    assert sdi.dlrm_read_error(flag) == 0
+    samples = _chosen_samples(cfg, offsets)
+    p_ref, p_mag = _oracle_pooled(cfg, offsets, indices, samples)
+    sel = torch.from_numpy(samples).to(DEV)
+    rel = REL[cfg["dtype"]]
+    assert_close(pooled[sel].cpu().numpy(), p_ref, p_mag, rel, "fused pooled")
+    y_ref, y_mag = oracle.interact_fwd(e0[samples], p_ref, inc, emb_mag=p_mag)
+    assert_close(y[sel].cpu().numpy(), y_ref, y_mag, rel, "fused y")
+
+
+def test_full_size_adagrad_multi_hot():
+    cfg = W.make_config("multi-hot")
+    _need(cfg, extra=0.5e9)
+    B, T, d = cfg["B"], cfg["T"], cfg["d"]
+    offsets, indices = W.make_indices(cfg)
+    tables = W.make_tables_device(cfg)
+    nnz = indices.size
+    dp_host = W.make_dpooled(cfg)
+    rng = np.random.default_rng(5)
+    state = [torch.from_numpy(rng.uniform(0.01, 2.0, r).astype(np.float32)).to(DEV) for r in cfg["rows"]]
+    state0 = [s.clone() for s in state]
+    ws = torch.empty(sdi.dlrm_emb_bag_bwd_workspace_size(T, B, nnz, d), dtype=torch.uint8, device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lr, eps = 0.05, 1e-6
+    view = sdi.dlrm_emb_bag_bwd_adagrad(tables, state, torch.from_numpy(offsets).to(DEV),
+                                        torch.from_numpy(indices).to(DEV), B, torch.from_numpy(dp_host).to(DEV), lr,
+                                        eps, ws, err_flag=flag, want_view=True)
+    assert sdi.dlrm_read_error(flag) == 0
+    co = oracle.coalesce(cfg["rows"], offsets, indices, B)
+    assert int(view["num_unique"].item()) == co["U"]
+    # sampled unique rows: the longest runs and random ones, as a sub-problem
+    lengths = np.diff(co["seg_off"])
+    us = np.unique(np.concatenate([np.argsort(lengths)[-12:], rng.integers(0, co["U"], 96)]))
+    starts, ends = co["seg_off"][us], co["seg_off"][us + 1]
+    sub = dict(U=us.size, uniq_table=co["uniq_table"][us], uniq_row=co["uniq_row"][us],
+               sorted_pos=np.concatenate([co["sorted_pos"][a:b] for a, b in zip(starts, ends)]),
+               seg_off=np.concatenate([[0], np.cumsum(ends - starts)]))
+    tabs, maps = _sub_tables(cfg, [sub["uniq_row"][sub["uniq_table"] == t] for t in range(T)])
+    s_in = np.array([state0[int(t)][int(r)].item() for t, r in zip(sub["uniq_table"], sub["uniq_row"])])
+    sub["uniq_row"] = np.array([np.searchsorted(maps[t], r) for t, r in zip(sub["uniq_table"], sub["uniq_row"])],
+                               dtype=np.int64)
+    _, _, s_ref, s_mag, w_ref, w_mag = oracle.adagrad(tabs, cfg["dtype"], offsets, B, nnz, dp_host.astype(np.float64),
+                                                      lr, eps, s_in, sub)
+    got_s = np.array([state[int(t)][int(r)].item() for t, r in zip(co["uniq_table"][us], co["uniq_row"][us])])
+    assert_close(got_s, s_ref, s_mag, REL["f32"], "accumulators")
+    got_w = np.stack([device_table_f64(tables[int(t)][int(r):int(r) + 1], cfg["dtype"])[0]
+                      for t, r in zip(co["uniq_table"][us], co["uniq_row"][us])])
+    assert_close(got_w, w_ref, w_mag, REL[cfg["dtype"]], "updated rows", table_dtype=cfg["dtype"])
+
+
+def test_full_size_int4_capacity():
+    cfg = W.make_config("capacity")
+    _need(cfg, extra=W.table_bytes(cfg) / 6)
+    B, T, d = cfg["B"], cfg["T"], cfg["d"]
+    offsets, indices = W.make_indices(cfg)
+    tables = W.make_tables_device(cfg)
+    q = [sdi.dlrm_quantize_int4(t) for t in tables]
+    del tables
+    gc.collect()
+    torch.cuda.empty_cache()
+    out = torch.empty((B, T, d), device=DEV)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sdi.dlrm_emb_bag_fwd(q, torch.from_numpy(offsets).to(DEV), torch.from_numpy(indices).to(DEV), B, out,
+                         err_flag=flag, d=d)
+    assert sdi.dlrm_read_error(flag) == 0
+    samples = _chosen_samples(cfg, offsets)
+    bags = [[indices[offsets[t * B + b]:offsets[t * B + b + 1]] for b in samples] for t in range(T)]
+    tabs, maps = _sub_tables(cfg, [np.concatenate(bt) for bt in bags])
+    # the device's codes of the touched rows are the oracle's encoding of the generated rows
+    qsub = []
+    for t in range(T):
+        qt = oracle.quantize_int4(tabs[t], cfg["dtype"])
+        got = q[t][torch.from_numpy(maps[t]).to(DEV)].cpu().numpy()
+        np.testing.assert_array_equal(got, qt)
+        qsub.append(qt)
+    sub_off, sub_idx = [0], []
+    for t in range(T):
+        for bag in bags[t]:
+            sub_idx.append(np.searchsorted(maps[t], bag))
+            sub_off.append(sub_off[-1] + bag.size)
+    ref, mag = oracle.emb_bag_fwd(qsub, "int4", np.array(sub_off), np.concatenate(sub_idx), len(samples), d=d)
+    assert_close(out[torch.from_numpy(samples).to(DEV)].cpu().numpy(), ref, mag, REL["f32"], "int4 pooled")
