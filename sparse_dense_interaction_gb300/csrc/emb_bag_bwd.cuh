@@ -14,7 +14,7 @@ constexpr int kRadix = 1 << kRadixBits;
 constexpr int kMaxPasses = 4;
 constexpr uint32_t kSentinel = 0xffffffffu;   // sort key of an out-of-range index
 constexpr uint32_t kHasHead = 1u, kHeadEnds = 2u, kHasTail = 4u;
-constexpr int kReduceThreads = 256;           // 8 warps per tile in the reduce, one chunk each
+constexpr int kReduceThreads = 256;           // 8 warps per tile in the reduce, one or two chunks each
 constexpr int kFinalizeBlock = 32;            // chunks summed per block in the finalize's first level
 
 // Reduce chunks per tile (the layout of the partial sums is sized for it):

@@ -4,7 +4,9 @@
 // Interaction Layer": one dot product per pair of the vectors
 // {e0, e_1 .. e_N}, self pairs optional, the terms concatenated with e0.
 //
-// Forward design: a CTA takes S samples.  The F x d block Z of each sample
+// Forward design (operands the bulk tensor copy cannot describe; the usual
+// path is interact_tma.cu, same arithmetic): a CTA takes S samples.  The F x d
+// block Z of each sample
 // (row 0 = e0, rows 1..N = pooled embeddings) is staged through shared memory
 // in chunks of KC = 32 columns: each row chunk is one coalesced 128-byte read
 // (4 lanes x 32 bytes), transposed to [k][i] (column groups XOR-swizzled by k
@@ -14,7 +16,8 @@
 // chunks (16 FMAs per two 16-byte shared loads; lanes of a warp share tile
 // rows and columns, so those loads are broadcasts).  The triangle is staged
 // in shared memory and written out as one contiguous, coalesced row per
-// sample; the e0 copy is written while Z is loaded.
+// sample; the e0 copy (and, in the alongside layout, each pooled row) is
+// written while Z is loaded.
 //
 // Backward design: dZ = (G + G^T) Z with G the lower-triangular matrix of
 // upstream gradients.  A CTA takes S samples, expands dy into the symmetric
@@ -22,7 +25,8 @@
 // columns; each thread owns a 4-row x 4-column tile of dZ and loops over the
 // F rows of the chunk (a broadcast 16-byte load of four G entries and a
 // conflict-free 16-byte load of four Z entries per 16 FMAs).  dZ rows go
-// straight to de0 (plus the e0 part of dy) and to the pooled gradients.
+// straight to de0 (plus the e0 part of dy) and to the pooled gradients (plus
+// their copies' part of dy in the alongside layout).
 #include "interact.cuh"
 
 namespace dlrm {

@@ -1,22 +1,26 @@
 // Segmented reduce of pooled-vector gradients over runs of equal rows, and
-// the row-wise SGD update of each unique row (the embedding-bag backward of
+// the row-wise update of each unique row (the embedding-bag backward of
 // "Notes/DLRM", vault-aram.pages.dev: section 2's per-feature lookups are
 // summed, so every lookup of a row receives its bag's pooled gradient;
-// section 5: the rows are then trained, here by plain SGD).
+// section 5: the rows are then trained by an optimizer -- plain SGD, or
+// row-wise AdaGrad).
 //
 // Design.  One CTA per sort tile (4096 sorted lookups of one table):
 //  A. the CTA stages the tile's sorted rows and, through the position of each
 //     lookup, its bag id in shared memory, marks where runs of equal rows
 //     start, counts the starts of every chunk and numbers the runs;
-//  B. each warp walks one chunk of 512 sorted lookups; a lane owns one 16-byte
-//     piece of each pooled-gradient row (32 lanes x 16 B = 128 fp32 values
-//     per pass), 4 rows in flight, fp32 sums with packed adds.  The kernel
-//     is kept lean (at most 64 registers, so 4 CTAs of 8 warps share an SM and
-//     hide the latency of the row gathers); when a run ends its table row
-//     is read, updated (w - lr*g, one rounding to the table type) and
-//     written, once per unique row.  Runs that cross a chunk boundary leave
-//     partial sums, which two small kernels combine in chunk order (block
-//     sums of 32 chunks, then the run's owner), so results are deterministic.
+//  B. a stream of G lanes walks one chunk of sorted lookups (for d >= 128: 16
+//     streams of 16 lanes, 256 lookups each; a lane owns two 16-byte pieces
+//     of each pooled-gradient row), 2 rows in flight, fp32 sums with packed
+//     adds; the table rows of runs starting a step ahead are prefetched into
+//     L2.  The kernel is kept lean (at most 64 registers, so 4 CTAs of 8
+//     warps share an SM and hide the latency of the row gathers); when a run
+//     ends its table row is read, updated (SGD: w - lr*g; AdaGrad: the row's
+//     sum of squares reduced over the stream, the accumulator updated once,
+//     w - lr*g/(sqrt(s')+eps); one rounding to the table type) and written,
+//     once per unique row.  Runs that cross a chunk boundary leave partial
+//     sums, which two small kernels combine in chunk order (block sums of 32
+//     chunks, then the run's owner), so results are deterministic.
 #include <type_traits>
 
 #include "emb_bag_bwd.cuh"
