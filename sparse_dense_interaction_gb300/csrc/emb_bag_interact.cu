@@ -273,11 +273,8 @@ static int launch_fused(const TableSet &ts, int T, int d, int nchunks, const int
     constexpr int U0 = (C == 1 ? 8 : (C == 2 ? 4 : 2)) / ((Chunk16<TT>::kElems == 8 && C > 1) ? 2 : 1);
     constexpr int U = U0 < G ? U0 : G;
     auto kernel = emb_bag_interact_fwd_kernel<TT, G, C, U>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax);
-        attr_set = true;
-    }
+    // set at every launch: cheap, thread-safe and right for whichever device is current
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax);
     const int64_t grid = (B + fs.S - 1) / fs.S;
     kernel<<<(unsigned)grid, fs.threads, fs.smem, st>>>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s,
                                                         mode, y, ys, pooled, pss, pts, fs.S, fs.KS, err);

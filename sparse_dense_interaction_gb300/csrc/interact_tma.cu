@@ -275,17 +275,16 @@ interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __gri
 // link against the driver library).
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once (a function-local static is initialised thread-safely)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -340,11 +339,8 @@ int launch_interact_fwd_tma(const float *e0, int64_t e0s, const float *emb, int6
     if (smem > 112 * 1024 || (int64_t)S * KS * ntiles > 512)  // two CTAs of up to 512 threads per SM
         return 1;
     const int threads = ((S * KS * ntiles + 31) / 32) * 32;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(interact_fwd_tma_kernel<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        attr_set = true;
-    }
+    // set at every launch: cheap, thread-safe and right for whichever device is current
+    cudaFuncSetAttribute(interact_fwd_tma_kernel<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     const int64_t grid = (B + S - 1) / S;
     interact_fwd_tma_kernel<KS><<<(unsigned)grid, threads, smem, st>>>(map_emb, map_e0, N, d, B, mode, y, ys, S, R8);
     count_launch(st);
