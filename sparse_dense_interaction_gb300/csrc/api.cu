@@ -24,6 +24,20 @@ void count_launch(cudaStream_t st)
 
 int launch_status() { return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA; }
 
+int allow_dynamic_smem(const void *kernel, int bytes, std::atomic<unsigned long long> *done)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;  // devices past 64: set every time
+    if (bit && (done->load(std::memory_order_acquire) & bit))
+        return DLRM_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    done->fetch_or(bit, std::memory_order_release);
+    return DLRM_OK;
+}
+
 int sm_count()
 {
     int dev = 0, n = 0;

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "dlrm_sparse.h"
 
 namespace dlrm {
@@ -24,6 +26,10 @@ void count_launch(cudaStream_t st);
 int launch_status();
 // Streaming multiprocessor count of the current device.
 int sm_count();
+// Raises a kernel's dynamic shared-memory limit on the current device, once
+// per device and kernel (`done` is the kernel's bit mask of devices already
+// set; concurrent callers may both set it, which is harmless).
+int allow_dynamic_smem(const void *kernel, int bytes, std::atomic<unsigned long long> *done);
 
 __device__ __forceinline__ void raise_flag(int32_t *flag, int bits)
 {

@@ -273,8 +273,9 @@ static int launch_fused(const TableSet &ts, int T, int d, int nchunks, const int
     constexpr int U0 = (C == 1 ? 8 : (C == 2 ? 4 : 2)) / ((Chunk16<TT>::kElems == 8 && C > 1) ? 2 : 1);
     constexpr int U = U0 < G ? U0 : G;
     auto kernel = emb_bag_interact_fwd_kernel<TT, G, C, U>;
-    // set at every launch: cheap, thread-safe and right for whichever device is current
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax);
+    static std::atomic<unsigned long long> smem_set{0};  // devices whose limit has been raised
+    if (allow_dynamic_smem(reinterpret_cast<const void *>(kernel), (int)kFusedSmemMax, &smem_set) != DLRM_OK)
+        return DLRM_ERR_CUDA;
     const int64_t grid = (B + fs.S - 1) / fs.S;
     kernel<<<(unsigned)grid, fs.threads, fs.smem, st>>>(ts, T, d, nchunks, offsets, indices, nnz, B, e0, e0s,
                                                         mode, y, ys, pooled, pss, pts, fs.S, fs.KS, err);

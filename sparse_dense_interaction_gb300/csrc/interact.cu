@@ -337,8 +337,10 @@ int launch_interact_fwd(const float *e0, int64_t e0s, const float *emb, int64_t 
     const int vec_out = aligned16(y) && ys % 4 == 0;
     const int64_t grid = (B + S - 1) / S;
     auto kernel = TS == 32 ? interact_fwd_kernel<32> : (TS == 64 ? interact_fwd_kernel<64> : interact_fwd_kernel<128>);
-    // set at every launch: cheap, thread-safe and right for whichever device is current
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    static std::atomic<unsigned long long> smem_set[3];  // per row width: devices whose limit has been raised
+    if (allow_dynamic_smem(reinterpret_cast<const void *>(kernel), 200 * 1024,
+                           &smem_set[TS == 32 ? 0 : (TS == 64 ? 1 : 2)]) != DLRM_OK)
+        return DLRM_ERR_CUDA;
     kernel<<<(unsigned)grid, threads, smem, st>>>(e0, e0s, emb, embs, N, d, B, mode, y, ys, S, vec_in, vec_out);
     count_launch(st);
     return launch_status();
@@ -360,8 +362,9 @@ int launch_interact_bwd(const float *e0, int64_t e0s, const float *emb, int64_t 
         S = (int)B;
     const int threads = ((S * items + 31) / 32) * 32;
     const size_t smem = (size_t)S * per_sample;
-    // set at every launch: cheap, thread-safe and right for whichever device is current
-    cudaFuncSetAttribute(interact_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    static std::atomic<unsigned long long> smem_set{0};  // devices whose limit has been raised
+    if (allow_dynamic_smem(reinterpret_cast<const void *>(interact_bwd_kernel), 200 * 1024, &smem_set) != DLRM_OK)
+        return DLRM_ERR_CUDA;
     const int vec_in = d % 4 == 0 && aligned16(e0) && aligned16(emb) && e0s % 4 == 0 && embs % 4 == 0;
     const int vec_out = d % 4 == 0 && aligned16(de0) && aligned16(demb) && de0s % 4 == 0 && dembs % 4 == 0;
     const int64_t grid = (B + S - 1) / S;

@@ -339,8 +339,10 @@ int launch_interact_fwd_tma(const float *e0, int64_t e0s, const float *emb, int6
     if (smem > 112 * 1024 || (int64_t)S * KS * ntiles > 512)  // two CTAs of up to 512 threads per SM
         return 1;
     const int threads = ((S * KS * ntiles + 31) / 32) * 32;
-    // set at every launch: cheap, thread-safe and right for whichever device is current
-    cudaFuncSetAttribute(interact_fwd_tma_kernel<KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    static std::atomic<unsigned long long> smem_set{0};  // devices whose limit has been raised
+    if (allow_dynamic_smem(reinterpret_cast<const void *>(interact_fwd_tma_kernel<KS>), 200 * 1024, &smem_set) !=
+        DLRM_OK)
+        return DLRM_ERR_CUDA;
     const int64_t grid = (B + S - 1) / S;
     interact_fwd_tma_kernel<KS><<<(unsigned)grid, threads, smem, st>>>(map_emb, map_e0, N, d, B, mode, y, ys, S, R8);
     count_launch(st);
