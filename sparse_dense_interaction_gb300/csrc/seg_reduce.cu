@@ -553,17 +553,24 @@ template <typename TT>
 static int reduce_typed(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
 {
     if (a.opt == kOptAdagrad) {
-        // a stream holds the whole row: up to 128 (16 x 2 x 4 or 32 x 1 x 4),
-        // 256 (32 x 2 x 4) or 256 (32 x 8 x 1, scalar) elements
+        // a stream holds the whole row: up to 128 (16 x 2 x 4), 256 (32 x 2 x 4)
+        // or 256 (32 x 8 x 1, scalar) elements
         if (!vec)
             return run_reduce<TT, 1, 32, 8, 2, 0>(a, w, grid, st);
         if (a.d > 128)
             return run_reduce<TT, 4, 32, 2, 2, 1>(a, w, grid, st);
-    } else if (!vec) {
-        return run_reduce<TT, 1, 32, 1, 8, 0>(a, w, grid, st);
+        return run_reduce<TT, 4, 16, 2, 2, 1>(a, w, grid, st);
     }
-    // rows of 32+ pieces: half-warp streams with two pieces per lane
-    return a.d >= 128 ? run_reduce<TT, 4, 16, 2, 2, 1>(a, w, grid, st) : run_reduce<TT, 4, 32, 1, 4, 1>(a, w, grid, st);
+    if (!vec)
+        return run_reduce<TT, 1, 32, 1, 8, 0>(a, w, grid, st);
+    // 16-lane streams (more chunks per tile, shorter serial walks): two
+    // 16-byte pieces per lane for rows of 128+ values, one for rows of up to
+    // 64; rows in between keep one 32-lane stream per chunk (a single walk)
+    if (a.d >= 128)
+        return run_reduce<TT, 4, 16, 2, 2, 1>(a, w, grid, st);
+    if (a.d <= 64)
+        return run_reduce<TT, 4, 16, 1, 2, 1>(a, w, grid, st);
+    return run_reduce<TT, 4, 32, 1, 4, 1>(a, w, grid, st);
 }
 
 int launch_seg_reduce(int dtype, const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
