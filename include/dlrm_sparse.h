@@ -188,6 +188,24 @@ int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb,
                       float *demb, int64_t demb_sample_stride, dlrm_stream_t stream);
 
 /*
+ * Kernel family of dlrm_interact_fwd and dlrm_interact_bwd (a process-wide
+ * setting, for benchmarking and testing the alternatives).
+ * DLRM_INTERACT_KERNEL_AUTO (the default): the tensor-core kernels where they
+ * apply -- 16-byte aligned operands, d and the row strides multiples of 4 --
+ * else the CUDA-core kernels.  The tensor-core kernels run TF32 MMAs on a
+ * hi + lo split of every fp32 operand, which carries each product z_i.z_j to
+ * about 2^-21 of |z_i||z_j|, with fp32 accumulation.
+ * DLRM_INTERACT_KERNEL_CUDA_CORE: always the CUDA-core kernels (fp32 FMAs).
+ * dlrm_set_interact_kernel returns DLRM_OK, or DLRM_ERR_INVALID_ARG for an
+ * unknown value (the setting is then unchanged); calls already enqueued are
+ * not affected.  dlrm_get_interact_kernel returns the setting.
+ */
+#define DLRM_INTERACT_KERNEL_AUTO 0
+#define DLRM_INTERACT_KERNEL_CUDA_CORE 1
+int dlrm_set_interact_kernel(int kind);
+int dlrm_get_interact_kernel(void);
+
+/*
  * Embedding-bag forward and interaction forward in one call ("Notes/DLRM",
  * section 3: the interaction directly follows the lookups).  Computes what
  * dlrm_emb_bag_fwd followed by dlrm_interact_fwd with N = T computes:

@@ -42,6 +42,8 @@ SIGNATURES = {
     "dlrm_interact_fwd": (_i32, [_vp, _i64, _vp, _i64, _i32, _i32, _i64, _i32, _vp, _i64, _vp]),
     "dlrm_interact_bwd": (_i32, [_vp, _i64, _vp, _i64, _i32, _i32, _i64, _i32, _vp, _i64, _vp,
                                  _i64, _vp, _i64, _vp]),
+    "dlrm_set_interact_kernel": (_i32, [_i32]),
+    "dlrm_get_interact_kernel": (_i32, []),
     "dlrm_emb_bag_bwd_workspace_size": (_sz, [_i32, _i64, _i64, _i32]),
     "dlrm_emb_bag_bwd_sgd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64,
                                     _i64, _f32, _vp, _i64, _vp, _sz, ctypes.POINTER(CoalescedView),
@@ -168,6 +170,17 @@ def dlrm_num_pairs(N: int, include_self: bool) -> int:
 
 
 INTERACT_SELF, INTERACT_ALONGSIDE = 1, 2
+INTERACT_KERNEL_AUTO, INTERACT_KERNEL_CUDA_CORE = 0, 1
+
+
+def dlrm_set_interact_kernel(kind: int) -> None:
+    """Kernel family of the interaction calls: INTERACT_KERNEL_AUTO (tensor cores
+    where they apply) or INTERACT_KERNEL_CUDA_CORE (process-wide)."""
+    _check(load().dlrm_set_interact_kernel(int(kind)), "dlrm_set_interact_kernel")
+
+
+def dlrm_get_interact_kernel() -> int:
+    return int(load().dlrm_get_interact_kernel())
 
 
 def _mode(include_self, alongside):

@@ -47,6 +47,10 @@ int sm_count()
     return n;
 }
 
+static std::atomic<int> g_interact_kernel{DLRM_INTERACT_KERNEL_AUTO};
+
+bool interact_tensor_cores() { return g_interact_kernel.load(std::memory_order_relaxed) == DLRM_INTERACT_KERNEL_AUTO; }
+
 // kernels (defined in the other translation units)
 bool emb_bag_fwd_vectorisable(const TableSet &, int, int, int, const float *, int64_t, int64_t);
 int64_t int4_row_bytes(int);
@@ -204,6 +208,16 @@ int64_t dlrm_interact_width(int N, int d, int mode)
     return (int64_t)d * ((mode & DLRM_INTERACT_ALONGSIDE) ? (int64_t)N + 1 : 1) +
            dlrm_num_pairs(N, mode & DLRM_INTERACT_SELF);
 }
+
+int dlrm_set_interact_kernel(int kind)
+{
+    if (kind != DLRM_INTERACT_KERNEL_AUTO && kind != DLRM_INTERACT_KERNEL_CUDA_CORE)
+        return DLRM_ERR_INVALID_ARG;
+    dlrm::g_interact_kernel.store(kind, std::memory_order_relaxed);
+    return DLRM_OK;
+}
+
+int dlrm_get_interact_kernel(void) { return dlrm::g_interact_kernel.load(std::memory_order_relaxed); }
 
 int dlrm_interact_fwd(const float *e0, int64_t e0_stride, const float *emb, int64_t emb_sample_stride,
                       int N, int d, int64_t B, int mode, float *y, int64_t y_stride,

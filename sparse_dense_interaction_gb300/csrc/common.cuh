@@ -30,6 +30,9 @@ int sm_count();
 // per device and kernel (`done` is the kernel's bit mask of devices already
 // set; concurrent callers may both set it, which is harmless).
 int allow_dynamic_smem(const void *kernel, int bytes, std::atomic<unsigned long long> *done);
+// Whether the interaction calls may take the tensor-core kernels (the
+// process-wide setting of dlrm_set_interact_kernel).
+bool interact_tensor_cores();
 
 __device__ __forceinline__ void raise_flag(int32_t *flag, int bits)
 {

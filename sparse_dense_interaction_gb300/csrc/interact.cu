@@ -310,11 +310,21 @@ static bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 1
 
 int launch_interact_fwd_tma(const float *, int64_t, const float *, int64_t, int, int, int64_t, int, float *,
                             int64_t, cudaStream_t);
+int launch_interact_fwd_tc(const float *, int64_t, const float *, int64_t, int, int, int64_t, int, float *,
+                           int64_t, cudaStream_t);
+int launch_interact_bwd_tc(const float *, int64_t, const float *, int64_t, int, int, int64_t, int, const float *,
+                           int64_t, float *, int64_t, float *, int64_t, cudaStream_t);
 
 int launch_interact_fwd(const float *e0, int64_t e0s, const float *emb, int64_t embs, int N, int d,
                         int64_t B, int mode, float *y, int64_t ys, cudaStream_t st)
 {
-    // the bulk-tensor-copy kernel when the copy engine can describe the operands
+    // the tensor-core kernel where it applies, else the bulk-tensor-copy
+    // kernel when the copy engine can describe the operands
+    if (interact_tensor_cores()) {
+        const int r = launch_interact_fwd_tc(e0, e0s, emb, embs, N, d, B, mode, y, ys, st);
+        if (r != 1)
+            return r;
+    }
     const int r = launch_interact_fwd_tma(e0, e0s, emb, embs, N, d, B, mode, y, ys, st);
     if (r != 1)
         return r;
@@ -350,6 +360,11 @@ int launch_interact_bwd(const float *e0, int64_t e0s, const float *emb, int64_t 
                         int64_t B, int mode, const float *dy, int64_t dys, float *de0, int64_t de0s,
                         float *demb, int64_t dembs, cudaStream_t st)
 {
+    if (interact_tensor_cores()) {
+        const int r = launch_interact_bwd_tc(e0, e0s, emb, embs, N, d, B, mode, dy, dys, de0, de0s, demb, dembs, st);
+        if (r != 1)
+            return r;
+    }
     const int F = N + 1;
     const int Fp = (F + 3) & ~3;
     const int nTR = Fp / 4;

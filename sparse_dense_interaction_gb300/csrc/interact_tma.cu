@@ -272,8 +272,8 @@ interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __gri
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up through the runtime (no
-// link against the driver library).
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+// link against the driver library); null if the driver has none.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
     // looked up once (a function-local static is initialised thread-safely)
     static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
@@ -297,7 +297,7 @@ int launch_interact_fwd_tma(const float *e0, int64_t e0s, const float *emb, int6
     auto al16 = [](const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
     if (N < 1 || d % 4 != 0 || e0s % 4 != 0 || embs % 4 != 0 || !al16(e0) || !al16(emb) || B > 0x7fffffff)
         return 1;
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc)
         return 1;
     CUtensorMap map_emb, map_e0;

@@ -164,6 +164,14 @@ def test_backward_rejects_bad_arguments(lib):
     assert lib.dlrm_kernel_launch_count() == 0
 
 
+def test_interaction_kernel_setting(lib):
+    assert lib.dlrm_get_interact_kernel() == 0  # tensor cores where they apply
+    assert lib.dlrm_set_interact_kernel(1) == 0 and lib.dlrm_get_interact_kernel() == 1
+    assert lib.dlrm_set_interact_kernel(7) == _native.ERR_INVALID_ARG and lib.dlrm_get_interact_kernel() == 1
+    assert lib.dlrm_set_interact_kernel(-1) == _native.ERR_INVALID_ARG
+    assert lib.dlrm_set_interact_kernel(0) == 0 and lib.dlrm_get_interact_kernel() == 0
+
+
 def test_read_error_needs_a_flag(lib):
     assert lib.dlrm_read_error(None, None) == _native.ERR_INVALID_ARG
     assert lib.dlrm_clear_error(None, None) == _native.ERR_INVALID_ARG

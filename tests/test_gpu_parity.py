@@ -130,10 +130,26 @@ def test_emb_bag_fwd_bad_offsets_are_flagged():
 # ----------------------------------------------------------- interaction ---
 
 INTER_CASES = [  # (B, N, d, include_self)
-    (300, 26, 128, False), (300, 26, 64, False), (128, 8, 16, False), (37, 100, 256, True),
+    (300, 26, 128, False), (301, 26, 64, False), (128, 8, 16, False), (37, 100, 256, True),
     (40, 127, 32, True), (50, 0, 16, False), (50, 0, 16, True), (33, 1, 8, True),
     (65, 5, 3, False), (21, 13, 33, True), (1, 26, 128, False),
+    # 64-row and 128-row sample blocks of the tensor-core kernel, a last chunk of 8 columns
+    (77, 40, 64, False), (19, 63, 40, True), (23, 64, 96, False),
+    # more tiles than SMs: the persistent loop wraps its staging ring and both accumulators
+    (5001, 26, 128, False), (700, 100, 256, True),
+    # enough units for the tensor-core backward: 16-row Gs, two d tiles, a ragged d tile
+    (5000, 13, 64, True), (4900, 31, 256, False), (2500, 20, 200, True),
 ]
+
+KERNELS = {"auto": sdi.INTERACT_KERNEL_AUTO, "cuda-core": sdi.INTERACT_KERNEL_CUDA_CORE}
+
+
+@pytest.fixture(params=list(KERNELS))
+def kernel(request):
+    """Runs the test with the interaction kernels of each family."""
+    sdi.dlrm_set_interact_kernel(KERNELS[request.param])
+    yield request.param
+    sdi.dlrm_set_interact_kernel(sdi.INTERACT_KERNEL_AUTO)
 
 
 def _inter_inputs(B, N, d, inc, seed=0):
@@ -145,7 +161,7 @@ def _inter_inputs(B, N, d, inc, seed=0):
 
 
 @pytest.mark.parametrize("B,N,d,inc", INTER_CASES)
-def test_interact_fwd_matches_oracle(B, N, d, inc):
+def test_interact_fwd_matches_oracle(B, N, d, inc, kernel):
     e0, emb, _ = _inter_inputs(B, N, d, inc)
     width = d + sdi.dlrm_num_pairs(N, inc)
     y = torch.full((B, width), float("nan"), device=DEV)
@@ -158,7 +174,7 @@ def test_interact_fwd_matches_oracle(B, N, d, inc):
 
 
 @pytest.mark.parametrize("B,N,d,inc", INTER_CASES)
-def test_interact_bwd_matches_oracle(B, N, d, inc):
+def test_interact_bwd_matches_oracle(B, N, d, inc, kernel):
     e0, emb, dy = _inter_inputs(B, N, d, inc)
     de0 = torch.full((B, d), float("nan"), device=DEV)
     demb = torch.full((B, N, d), float("nan"), device=DEV)
@@ -169,7 +185,7 @@ def test_interact_bwd_matches_oracle(B, N, d, inc):
     assert_close(demb.cpu().numpy(), r_demb, m_demb, REL["f32"], "demb")
 
 
-def test_interact_with_padded_rows():
+def test_interact_with_padded_rows(kernel):
     # row strides wider than the rows (e0 and y inside larger buffers)
     B, N, d = 70, 9, 24
     e0, emb, dy = _inter_inputs(B, N, d, False)
@@ -183,12 +199,33 @@ def test_interact_with_padded_rows():
     assert torch.all(y_big[:, d + P:] == -1.0)
 
 
+@pytest.mark.parametrize("B,N,d,inc", [(5000, 26, 128, False), (40, 100, 256, True)])
+def test_interact_rows_of_very_different_scales(B, N, d, inc, kernel):
+    # the error bound is relative to sum |z_i||z_j|: rows scaled by 1e-3 .. 1e3,
+    # elements spanning 6 decades within a row
+    rng = np.random.default_rng([11, B, N, d])
+    e0 = (rng.standard_normal((B, d)) * 10.0 ** rng.uniform(-3, 3, (B, d))).astype(np.float32)
+    emb = (rng.standard_normal((B, N, d)) * 10.0 ** rng.uniform(-3, 3, (B, N, 1))
+           * 10.0 ** rng.uniform(-3, 3, (B, N, d))).astype(np.float32)
+    dy = rng.standard_normal((B, d + oracle.num_pairs(N, inc))).astype(np.float32)
+    y = torch.full((B, d + sdi.dlrm_num_pairs(N, inc)), float("nan"), device=DEV)
+    sdi.dlrm_interact_fwd(_t(e0), _t(emb), inc, y)
+    ref, mag = oracle.interact_fwd(e0, emb, inc)
+    assert_close(y.cpu().numpy(), ref, mag, REL["f32"], "fwd, wide range")
+    de0 = torch.full((B, d), float("nan"), device=DEV)
+    demb = torch.full((B, N, d), float("nan"), device=DEV)
+    sdi.dlrm_interact_bwd(_t(e0), _t(emb), inc, _t(dy), de0, demb)
+    r_de0, m_de0, r_demb, m_demb = oracle.interact_bwd(e0, emb, dy, inc)
+    assert_close(de0.cpu().numpy(), r_de0, m_de0, REL["f32"], "de0, wide range")
+    assert_close(demb.cpu().numpy(), r_demb, m_demb, REL["f32"], "demb, wide range")
+
+
 ALONG_CASES = [(300, 26, 128, False), (37, 100, 256, True), (65, 5, 3, False), (21, 13, 33, True),
-               (50, 0, 16, True), (33, 1, 8, False)]
+               (50, 0, 16, True), (33, 1, 8, False), (5000, 26, 128, True)]
 
 
 @pytest.mark.parametrize("B,N,d,inc", ALONG_CASES)
-def test_interact_alongside_matches_oracle(B, N, d, inc):
+def test_interact_alongside_matches_oracle(B, N, d, inc, kernel):
     # [e0 | e_1 .. e_N | pairs]: forward and backward
     rng = np.random.default_rng([7, B, N, d, inc])
     e0 = rng.standard_normal((B, d), dtype=np.float32)
