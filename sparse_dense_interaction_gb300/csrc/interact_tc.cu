@@ -654,11 +654,330 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
     }
 }
 
+// ------------------------------------------------- backward, 33 to 128 vectors
+//
+// One unit = one sample and one tile of up to 128 columns of d.  The MMA
+// computes dZ transposed, M = 128, N = Np (F rounded up to 16), K = 8 per
+// instruction:
+//   D (tensor memory, lane m = column m of the tile) = Z^T . Gs,
+//   A = Z^T in tensor memory (lane m holds z_k[m], k = 0 .. F-1, e0 first),
+//   B = Gs = G + G^T in shared memory (row n holds Gs[n][k]; a self pair
+//     counts twice),
+// split hi + lo on both sides, three MMAs per K step (hi.hi + lo.hi +
+// hi.lo).  K runs in chunks of 32 vectors: a bulk tensor copy brings the
+// chunk's 32 raw rows of Z (unswizzled; the box starts one row before the
+// chunk, so for the first chunk its row 0 reads as zero and e0 comes in a row
+// of its own), 4-byte asynchronous copies bring the unit's pair gradients
+// once (a row of dy need not be 16-byte aligned).  The converters write the
+// chunk's A into tensor memory (no shared-memory write) and its columns of Gs
+// into shared memory (published to the tensor core by a proxy fence).
+// Accumulators of Np rounded up to 32 columns fill tensor-memory columns
+// 0 .. 255 (8, 4 or 2 of them), drained by two epilogue groups (warps 0..3
+// and 4..7, alternate units: the writes of dZ, row i as 32 consecutive floats
+// per warp, are the slow part); each loads the e0 part of dy of its next unit
+// ahead.  One converter group (warps 8..11).
+
+namespace {
+
+constexpr int kBwcEpiGroups = 2, kBwcConvWarp0 = 8, kBwcTmaWarp = 12, kBwcMmaWarp = 13;
+constexpr int kBwcThreads = 448;
+constexpr uint32_t kBwcACol = 256;  // A chunk slots at 256 + 64 a (hi at +0, lo at +32); accumulators below
+constexpr int kBwcMaxAS = 4;
+constexpr int kBwcMaxDS = 8;        // pair-gradient slots (units)
+constexpr int kBwcMaxAcc = 8;       // accumulators of W = Np rounded up to 32 columns in columns 0 .. 255
+
+}  // namespace
+
+__global__ void __launch_bounds__(kBwcThreads, 1)
+interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
+                               const __grid_constant__ CUtensorMap map_e0, int N, int d, int64_t B, int mode,
+                               const float *__restrict__ dy, int64_t dys, float *__restrict__ de0, int64_t de0s,
+                               float *__restrict__ demb, int64_t dembs, int Np, int bx, int NR, int AS, int DS)
+{
+    constexpr int kTmemCols = 512;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int aborted_s;
+    __shared__ __align__(8) uint64_t drain_bar;
+    volatile int *aborted = &aborted_s;
+
+    const int inc = mode & kInteractSelf;
+    const bool along = (mode & kInteractAlongside) != 0;
+    const int F = N + 1;
+    const int P = (int)num_pairs_of(F, inc);
+    const int nd = (d + 127) / 128;  // d tiles
+    const int nkc = (F + 31) / 32;   // K chunks of 32 vectors
+    const int64_t nunits = B * nd;
+    const int64_t poff = along ? (int64_t)F * d : d;  // first pair column of dy
+    const uint32_t rs = (uint32_t)bx * 4u;             // bytes of a raw row
+    const uint32_t zslot = (33u * rs + 1023u) & ~1023u;           // 32 chunk rows, then e0
+    const uint32_t dslot = ((uint32_t)P * 4u + 127u) & ~127u;     // the unit's pair gradients
+    const uint32_t bbytes = (uint32_t)Np * 128u;                  // one B half (hi or lo)
+    const uint32_t W = ((uint32_t)Np + 31u) & ~31u;               // accumulator width
+    const uint32_t nacc = 256u / W;                               // accumulators: 8, 4 or 2
+
+    unsigned char *zring = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);  // [NR]
+    unsigned char *bring = zring + (size_t)NR * zslot;                                     // [AS] B hi, B lo
+    unsigned char *dring = bring + (size_t)AS * 2 * bbytes;                                // [DS]
+    uint64_t *zfull = reinterpret_cast<uint64_t *>(dring + (size_t)DS * dslot);             // [NR]
+    uint64_t *zempty = zfull + NR;                                                         // [NR]
+    uint64_t *dfull = zempty + NR;                                                         // [DS]
+    uint64_t *dempty = dfull + DS;                                                         // [DS]
+    uint64_t *afull = dempty + DS;                                                         // [AS]
+    uint64_t *aempty = afull + AS;                                                         // [AS]
+    uint64_t *tfull = aempty + AS;                                                         // [nacc]
+    uint64_t *tempty = tfull + kBwcMaxAcc;                                                 // [nacc]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < NR; s++) {
+            tc::mbar_init(&zfull[s], 1);
+            tc::mbar_init(&zempty[s], 128);
+        }
+        for (int s = 0; s < DS; s++) {
+            tc::mbar_init(&dfull[s], 32);  // one copy arrival per lane of the copy warp
+            tc::mbar_init(&dempty[s], 128);
+        }
+        for (int s = 0; s < AS; s++) {
+            tc::mbar_init(&afull[s], 128);
+            tc::mbar_init(&aempty[s], 1);
+        }
+        for (uint32_t b = 0; b < nacc; b++) {
+            tc::mbar_init(&tfull[b], 1);
+            tc::mbar_init(&tempty[b], 128);
+        }
+        tc::mbar_init(&drain_bar, 1);
+        aborted_s = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == kBwcMmaWarp)
+        tc::tmem_alloc<kTmemCols>(&tmem_slot);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == kBwcTmaWarp) {
+        // ---- copies: per unit the pair gradients (all lanes, 4-byte asynchronous copies), per
+        // chunk the raw rows of Z (lane 0, bulk tensor copies)
+        uint32_t iu = 0, ic = 0;
+        bool stop = false;
+        for (int64_t u = blockIdx.x; u < nunits && !stop; u += gridDim.x, iu++) {
+            const int64_t b = u / nd;
+            const int x = (int)(u - b * nd) * 128;
+            const uint32_t ds = iu % (uint32_t)DS, dph = iu / (uint32_t)DS;
+            if (dph > 0 && !tc::mbar_wait(&dempty[ds], (dph - 1) & 1, aborted))
+                break;
+            unsigned char *dd = dring + (size_t)ds * dslot;
+            const float *src = dy + b * dys + poff;
+            for (int p = lane; p < P; p += 32)
+                tc::cp_async4(dd + p * 4, src + p, true);
+            tc::cp_async_arrive(&dfull[ds]);
+            for (int c = 0; c < nkc; c++, ic++) {
+                const uint32_t zs = ic % (uint32_t)NR, zph = ic / (uint32_t)NR;
+                if (zph > 0 && !tc::mbar_wait(&zempty[zs], (zph - 1) & 1, aborted)) {
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) {
+                    unsigned char *zd = zring + (size_t)zs * zslot;
+                    tc::mbar_expect_tx(&zfull[zs], (c == 0 ? 33u : 32u) * rs);
+                    // rows 32c - 1 .. 32c + 30 of the pooled block = vectors 32c .. 32c + 31
+                    tc::tma_load_3d(zd, &map_emb, x, 32 * c - 1, (int)b, &zfull[zs]);
+                    if (c == 0)
+                        tc::tma_load_2d(zd + 32 * rs, &map_e0, x, (int)b, &zfull[zs]);
+                }
+            }
+        }
+        tc::cp_async_wait_all();
+        if (*aborted && lane == 0)
+            for (uint32_t i = ic > (uint32_t)NR ? ic - NR : 0; i < ic; i++)
+                for (int k = 0; k < tc::kSpinLimit && !tc::mbar_try_wait(&zfull[i % NR], (i / NR) & 1); k++) {
+                }
+        __syncwarp();
+    } else if (warp >= kBwcConvWarp0 && warp < kBwcTmaWarp) {
+        // ---- converters: thread a writes A lane a; the Gs entries of a chunk are the 16-byte
+        // units e = a, a + 128, .. of the chunk's Np x 32 block (row e / 8, columns 4 (e % 8) ..)
+        const int a = tid - kBwcConvWarp0 * 32;
+        const uint32_t lane_base = (uint32_t)(warp & 3) * 32 << 16;
+        uint32_t iu = 0, ic = 0;
+        bool stop = false;
+        for (int64_t u = blockIdx.x; u < nunits && !stop; u += gridDim.x, iu++) {
+            const uint32_t ds = iu % (uint32_t)DS, dph = iu / (uint32_t)DS;
+            if (!tc::mbar_wait(&dfull[ds], dph & 1, aborted))
+                break;
+            const float *dyp = reinterpret_cast<const float *>(dring + (size_t)ds * dslot);
+            for (int c = 0; c < nkc; c++, ic++) {
+                const uint32_t zs = ic % (uint32_t)NR, zph = ic / (uint32_t)NR;
+                const uint32_t as = ic % (uint32_t)AS, av = ic / (uint32_t)AS;
+                if (!tc::mbar_wait(&zfull[zs], zph & 1, aborted)) {
+                    stop = true;
+                    break;
+                }
+                const unsigned char *raw = zring + (size_t)zs * zslot;
+                float zh[32], zl[32];
+#pragma unroll
+                for (int r = 0; r < 32; r++) {
+                    float z = 0.f;
+                    if (a < bx && 32 * c + r < F)
+                        z = *reinterpret_cast<const float *>(raw + (c == 0 && r == 0 ? 32 * rs : (uint32_t)r * rs) +
+                                                             a * 4);
+                    zh[r] = tc::tf32_round(z);
+                    zl[r] = tc::tf32_round(z - zh[r]);
+                }
+                tc::mbar_arrive(&zempty[zs]);
+                if (av > 0 && !tc::mbar_wait(&aempty[as], (av - 1) & 1, aborted)) {
+                    stop = true;
+                    break;
+                }
+                tc::fence_after_sync();
+                unsigned char *bh = bring + (size_t)as * 2 * bbytes;
+                const int sh = inc ? 1 : -1;  // row i of the pairs starts at i (i + sh) / 2
+                for (int e = a; e < Np * 8; e += 128) {
+                    const int n = e >> 3, q = e & 7;
+                    float h[4], l[4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const int k = 32 * c + 4 * q + j;
+                        float v = 0.f;
+                        if (n < F && k < F && (n != k || inc)) {
+                            const int hi = n > k ? n : k, lo = n > k ? k : n;
+                            v = dyp[((hi * (hi + sh)) >> 1) + lo];
+                            if (n == k)
+                                v *= 2.f;  // a self pair counts in G and in G^T
+                        }
+                        h[j] = tc::tf32_round(v);
+                        l[j] = tc::tf32_round(v - h[j]);
+                    }
+                    *reinterpret_cast<float4 *>(bh + sw128(n, q)) = make_float4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<float4 *>(bh + bbytes + sw128(n, q)) = make_float4(l[0], l[1], l[2], l[3]);
+                }
+                const uint32_t ta = tmem + lane_base + kBwcACol + 64 * as;
+                tc::tmem_st32(ta, zh);
+                tc::tmem_st32(ta + 32, zl);
+                tc::fence_async_smem();
+                tc::tmem_st_wait();
+                tc::fence_before_sync();
+                tc::mbar_arrive(&afull[as]);
+                if (c == nkc - 1)
+                    tc::mbar_arrive(&dempty[ds]);  // the unit's pair gradients have been read
+            }
+        }
+    } else if (warp == kBwcMmaWarp) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::tf32_idesc(128, Np);
+            uint32_t iu = 0, ic = 0;
+            bool issued = false, ok = true;
+            for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, iu++) {
+                const uint32_t buf = iu % nacc, v = iu / nacc;
+                if (v > 0 && !tc::mbar_wait(&tempty[buf], (v - 1) & 1, aborted))
+                    break;
+                tc::fence_after_sync();
+                const uint32_t dt = tmem + buf * W;
+                for (int c = 0; c < nkc; c++, ic++) {
+                    const uint32_t as = ic % (uint32_t)AS, av = ic / (uint32_t)AS;
+                    if (!tc::mbar_wait(&afull[as], av & 1, aborted)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t ta = tmem + kBwcACol + 64 * as;
+                    const uint32_t bh = tc::smem_u32(bring + (size_t)as * 2 * bbytes), bl = bh + bbytes;
+                    const int ksteps = min(4, (F - 32 * c + 7) / 8);
+                    for (int kk = 0; kk < ksteps; kk++) {
+                        const uint64_t bhd = tc::sw128_desc(bh + 32u * kk), bld = tc::sw128_desc(bl + 32u * kk);
+                        const bool acc = c > 0 || kk > 0;
+                        tc::mma_tf32_ta(dt, ta + 8 * kk, bhd, idesc, acc);
+                        tc::mma_tf32_ta(dt, ta + 32 + 8 * kk, bhd, idesc, true);
+                        tc::mma_tf32_ta(dt, ta + 8 * kk, bld, idesc, true);
+                    }
+                    issued = true;
+                    tc::mma_commit(&aempty[as]);
+                }
+                if (!ok)
+                    break;
+                tc::mma_commit(&tfull[buf]);
+            }
+            if (*aborted && issued)
+                drain_mmas(&drain_bar);
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue: group g (warps 4g .. 4g + 3) takes units iu with iu % 2 == g; lane m of the
+        // accumulator = column m of the unit's d tile
+        const int g = warp >> 2, et = tid & 127;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        auto load_g0 = [&](int64_t u) -> float {
+            const int64_t b = u / nd;
+            const int m = (int)(u - b * nd) * 128 + et;
+            return (u < nunits && m < d) ? __ldg(dy + b * dys + m) : 0.f;
+        };
+        float g0n = load_g0(blockIdx.x + (int64_t)g * gridDim.x);
+        uint32_t iu = g;
+        for (int64_t u = blockIdx.x + (int64_t)g * gridDim.x; u < nunits;
+             u += kBwcEpiGroups * (int64_t)gridDim.x, iu += kBwcEpiGroups) {
+            const int64_t b = u / nd;
+            const int m = (int)(u - b * nd) * 128 + et;
+            const bool act = m < d;
+            const float g0 = g0n;
+            g0n = load_g0(u + kBwcEpiGroups * (int64_t)gridDim.x);
+            const uint32_t buf = iu % nacc;
+            const bool okw = tc::mbar_wait(&tfull[buf], (iu / nacc) & 1, aborted);
+            if (!__all_sync(0xffffffffu, okw))
+                break;
+            tc::fence_after_sync();
+            const uint32_t ta = tmem + lane_base + buf * W;
+            const float *dyb = dy + b * dys;
+            for (int c = 0; c < nkc; c++) {
+                float ga[32];
+#pragma unroll
+                for (int r = 0; r < 32; r++) {
+                    const int i = 32 * c + r;
+                    ga[r] = (along && act && i > 0 && i < F) ? __ldg(dyb + (int64_t)i * d + m) : 0.f;
+                }
+                float v[32];
+                tc::tmem_ld32(ta + 32 * c, v);
+                if (act) {
+#pragma unroll
+                    for (int r = 0; r < 32; r++) {
+                        const int i = 32 * c + r;
+                        if (i == 0)
+                            __stcs(de0 + b * de0s + m, v[0] + g0);
+                        else if (i < F)
+                            __stcs(demb + b * dembs + (int64_t)(i - 1) * d + m, v[r] + ga[r]);
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            tc::mbar_arrive(&tempty[buf]);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kBwcMmaWarp) {
+        tc::fence_after_sync();
+        tc::tmem_free<kTmemCols>(tmem);
+    }
+    if (*aborted) {
+        const float nan = __int_as_float(0x7fc00000);
+        for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+            const int64_t b = u / nd;
+            const int m0 = (int)(u - b * nd) * 128;
+            for (int m = m0 + tid; m < d && m < m0 + 128; m += blockDim.x) {
+                de0[b * de0s + m] = nan;
+                for (int i = 1; i < F; i++)
+                    demb[b * dembs + (int64_t)(i - 1) * d + m] = nan;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ launch
 //
 // Both return 1 (not launched) when the operands do not suit the kernels:
 // rows not of whole 16-byte chunks, unaligned bases or strides, no pooled
-// rows, more than 128 (forward) or 32 (backward) vectors per sample, rows
+// rows, more than 128 vectors per sample, rows
 // too short to fill the tiles (d < 32 forward, d < 64 backward), or too few
 // units to fill the backward's pipeline.  Otherwise they launch and return
 // the status.
@@ -717,11 +1036,86 @@ int launch_interact_fwd_tc(const float *e0, int64_t e0s, const float *emb, int64
     return launch_status();
 }
 
+static int launch_interact_bwd_tc_chunked(const float *e0, int64_t e0s, const float *emb, int64_t embs, int N,
+                                          int d, int64_t B, int mode, const float *dy, int64_t dys, float *de0,
+                                          int64_t de0s, float *demb, int64_t dembs, cudaStream_t st)
+{
+    const int F = N + 1;
+    const int64_t nunits = B * ((d + 127) / 128);
+    // d < 64 leaves most of a 128-lane tile idle, and with fewer than 32 units per SM the
+    // pipeline does not fill: the CUDA-core kernel is faster there
+    if (N < 1 || F > 128 || d < 64 || nunits < 32 * (int64_t)sm_count() || d % 4 != 0 || e0s % 4 != 0 ||
+        embs % 4 != 0 || !aligned16(e0) || !aligned16(emb) || B > 0x7fffffff)
+        return 1;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc)
+        return 1;
+    const int P = (int)num_pairs_of(F, mode & kInteractSelf);
+    const int Np = (F + 15) & ~15;
+    const int bx = d < 128 ? d : 128;  // columns of a d tile
+    CUtensorMap map_emb, map_e0;
+    std::memset(&map_emb, 0, sizeof map_emb);
+    std::memset(&map_e0, 0, sizeof map_e0);
+    const cuuint64_t dims3[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)B};
+    const cuuint64_t strides3[2] = {(cuuint64_t)d * 4, (cuuint64_t)embs * 4};
+    const cuuint32_t box3[3] = {(cuuint32_t)bx, 32, 1};  // 32 rows, zero-filled past the sample's N
+    const cuuint32_t one3[3] = {1, 1, 1};
+    const cuuint32_t one2[2] = {1, 1};
+    if (enc(&map_emb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(emb), dims3, strides3, box3, one3,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return 1;
+    const cuuint64_t dims_e0[2] = {(cuuint64_t)d, (cuuint64_t)B};
+    const cuuint64_t strides_e0[1] = {(cuuint64_t)e0s * 4};
+    const cuuint32_t box_e0[2] = {(cuuint32_t)bx, 1};
+    if (enc(&map_e0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(e0), dims_e0, strides_e0, box_e0, one2,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return 1;
+    const size_t zslot = (33 * (size_t)bx * 4 + 1023) & ~(size_t)1023;
+    const size_t dslot = ((size_t)P * 4 + 127) & ~(size_t)127;
+    const size_t bslot = 2 * (size_t)Np * 128;
+    const size_t fixed = 1024 + (size_t)kBwcMaxAcc * 16;
+    // operand slots: up to 4 (tensor memory), pair-gradient slots and raw chunks: as many as fit, up to 8
+    int AS = kBwcMaxAS, NR = 2, DS = 2;
+    auto total = [&](int as, int nr, int ds) {
+        return fixed + (size_t)as * (bslot + 16) + (size_t)nr * (zslot + 16) + (size_t)ds * (dslot + 16);
+    };
+    while (AS > 2 && total(AS, NR, DS) > kMaxSmem)
+        AS--;
+    for (bool grew = true; grew;) {
+        grew = false;
+        if (NR < 8 && total(AS, NR + 1, DS) <= kMaxSmem) {
+            NR++;
+            grew = true;
+        }
+        if (DS < kBwcMaxDS && total(AS, NR, DS + 1) <= kMaxSmem) {
+            DS++;
+            grew = true;
+        }
+    }
+    const size_t smem = total(AS, NR, DS);
+    if (smem > kMaxSmem)
+        return 1;
+    static std::atomic<unsigned long long> smem_set{0};
+    if (allow_dynamic_smem(reinterpret_cast<const void *>(interact_bwd_tc_chunked_kernel), (int)kMaxSmem, &smem_set) !=
+        DLRM_OK)
+        return DLRM_ERR_CUDA;
+    const int64_t grid = nunits < sm_count() ? nunits : sm_count();
+    interact_bwd_tc_chunked_kernel<<<(unsigned)grid, kBwcThreads, smem, st>>>(map_emb, map_e0, N, d, B, mode, dy, dys, de0,
+                                                                       de0s, demb, dembs, Np, bx, NR, AS, DS);
+    count_launch(st);
+    return launch_status();
+}
+
 int launch_interact_bwd_tc(const float *e0, int64_t e0s, const float *emb, int64_t embs, int N, int d, int64_t B,
                            int mode, const float *dy, int64_t dys, float *de0, int64_t de0s, float *demb,
                            int64_t dembs, cudaStream_t st)
 {
     const int F = N + 1;
+    if (F > 32)
+        return launch_interact_bwd_tc_chunked(e0, e0s, emb, embs, N, d, B, mode, dy, dys, de0, de0s, demb, dembs,
+                                              st);
     const int64_t nunits = B * ((d + 127) / 128);
     // d < 64 leaves most of a 128-lane tile idle, and with fewer than 32 units per SM the
     // pipeline does not fill: the CUDA-core kernel is faster there

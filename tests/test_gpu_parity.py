@@ -137,8 +137,10 @@ INTER_CASES = [  # (B, N, d, include_self)
     (77, 40, 64, False), (19, 63, 40, True), (23, 64, 96, False),
     # more tiles than SMs: the persistent loop wraps its staging ring and both accumulators
     (5001, 26, 128, False), (700, 100, 256, True),
-    # enough units for the tensor-core backward: 16-row Gs, two d tiles, a ragged d tile
-    (5000, 13, 64, True), (4900, 31, 256, False), (2500, 20, 200, True),
+    # enough units for the tensor-core backward: 16-row Gs, two d tiles, a ragged d tile, and
+    # two and three chunks of 32 vectors
+    (5000, 13, 64, True), (4900, 31, 256, False), (2500, 20, 200, True), (4900, 40, 64, False),
+    (4900, 70, 64, True),
 ]
 
 KERNELS = {"auto": sdi.INTERACT_KERNEL_AUTO, "cuda-core": sdi.INTERACT_KERNEL_CUDA_CORE}
@@ -183,6 +185,24 @@ def test_interact_bwd_matches_oracle(B, N, d, inc, kernel):
     r_de0, m_de0, r_demb, m_demb = oracle.interact_bwd(e0, emb, dy, inc)
     assert_close(de0.cpu().numpy(), r_de0, m_de0, REL["f32"], "de0")
     assert_close(demb.cpu().numpy(), r_demb, m_demb, REL["f32"], "demb")
+
+
+@pytest.mark.parametrize("B,N,d,inc", [(4870, 127, 64, True), (2440, 100, 256, True), (4870, 64, 128, False)])
+def test_interact_many_vectors_sampled(B, N, d, inc, kernel):
+    # 65 to 128 vectors per sample (four chunks of 32 in the tensor-core backward), against the
+    # oracle on sampled samples (first, last and a stride through the middle)
+    e0, emb, dy = _inter_inputs(B, N, d, inc, seed=4)
+    y = torch.full((B, d + sdi.dlrm_num_pairs(N, inc)), float("nan"), device=DEV)
+    sdi.dlrm_interact_fwd(_t(e0), _t(emb), inc, y)
+    de0 = torch.full((B, d), float("nan"), device=DEV)
+    demb = torch.full((B, N, d), float("nan"), device=DEV)
+    sdi.dlrm_interact_bwd(_t(e0), _t(emb), inc, _t(dy), de0, demb)
+    rows = np.unique(np.r_[0:24, B - 24:B, 0:B:97])
+    ref, mag = oracle.interact_fwd(e0[rows], emb[rows], inc)
+    assert_close(y.cpu().numpy()[rows], ref, mag, REL["f32"], f"fwd B={B} N={N} d={d}")
+    r_de0, m_de0, r_demb, m_demb = oracle.interact_bwd(e0[rows], emb[rows], dy[rows], inc)
+    assert_close(de0.cpu().numpy()[rows], r_de0, m_de0, REL["f32"], "de0")
+    assert_close(demb.cpu().numpy()[rows], r_demb, m_demb, REL["f32"], "demb")
 
 
 def test_interact_with_padded_rows(kernel):
