@@ -218,7 +218,8 @@ int dlrm_get_interact_kernel(void);
  * needs it; inference does not).  Arguments as in those two calls; pooled is
  * optional (NULL: not written), with strides in elements.  The pooled values
  * equal dlrm_emb_bag_fwd's bit for bit; y equals dlrm_interact_fwd's within
- * fp32 rounding (its dot products add their columns in another order).
+ * the accuracy of the two (fp32 dot products summed in another order, or the
+ * tensor-core split's 2^-20 of |z_i||z_j| per product).
  * T may be 1 .. 127.  The single-kernel path needs rows of a whole number of
  * 16-byte chunks up to 1 KB, 16-byte aligned tables (and pooled, with
  * strides that are multiples of 4), and a Z block of each sample that fits
