@@ -164,6 +164,10 @@ int64_t dlrm_interact_width(int N, int d, int mode);
  *       dlrm_emb_bag_fwd with out_table_stride = d).
  * y     device fp32 rows of dlrm_interact_width(N, d, mode), row stride
  *       y_stride.  N may be 0 .. 127.
+ * The kernels that stage operands through mbarrier-tracked copies wait only
+ * on their own CTA's copies and MMAs, and every such wait is bounded; should
+ * one run out, the samples of that CTA get NaN outputs (this call has no
+ * error flag), so a failure is visible rather than silent.
  */
 int dlrm_interact_fwd(const float *e0, int64_t e0_stride, const float *emb,
                       int64_t emb_sample_stride, int N, int d, int64_t B, int mode,
@@ -180,7 +184,8 @@ int dlrm_interact_fwd(const float *e0, int64_t e0_stride, const float *emb,
  *               + dy[b][i*d + e]   (alongside: the gradient of the copy)
  *
  * Inputs as in dlrm_interact_fwd; dy has row stride dy_stride, de0 row
- * stride de0_stride.  Outputs are overwritten (not accumulated).
+ * stride de0_stride.  Outputs are overwritten (not accumulated).  Bounded
+ * waits as in dlrm_interact_fwd (NaN outputs if one runs out).
  */
 int dlrm_interact_bwd(const float *e0, int64_t e0_stride, const float *emb,
                       int64_t emb_sample_stride, int N, int d, int64_t B, int mode,
