@@ -135,8 +135,7 @@ interact_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
     uint64_t *full = reinterpret_cast<uint64_t *>(ptab + ((P + 3) & ~3));  // [NS] bulk copies landed
     uint64_t *empty = full + NS;                                           // [NS] MMAs done with the slot
     uint64_t *afull = empty + NS;                                          // [kFwdAS] A written
-    uint64_t *aempty = afull + kFwdAS;                                     // [kFwdAS] MMAs done with A
-    uint64_t *tfull = aempty + kFwdAS;                                     // [2]
+    uint64_t *tfull = afull + kFwdAS;                                      // [2]
     uint64_t *tempty = tfull + 2;                                          // [2]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -158,10 +157,8 @@ interact_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
         }
-        for (int s = 0; s < kFwdAS; s++) {
+        for (int s = 0; s < kFwdAS; s++)
             tc::mbar_init(&afull[s], 128);
-            tc::mbar_init(&aempty[s], 1);
-        }
         for (int b = 0; b < 2; b++) {
             tc::mbar_init(&tfull[b], 1);
             tc::mbar_init(&tempty[b], 128);
@@ -269,9 +266,14 @@ interact_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
                     tv[k] = tc::tf32_trunc(v[k]);
                     lv[k] = tc::tf32_round(2.f * (v[k] - tv[k]));
                 }
-                if (av > 0 && !tc::mbar_wait(&aempty[as], (av - 1) & 1, aborted)) {
-                    stop = true;
-                    break;
+                // A slot `as` is free once the MMAs of item it - kFwdAS are done, which the B slot
+                // of that item signals (NS > kFwdAS, so that phase cannot have been passed)
+                if (av > 0) {
+                    const uint32_t j = it - kFwdAS;
+                    if (!tc::mbar_wait(&empty[j % (uint32_t)NS], (j / (uint32_t)NS) & 1, aborted)) {
+                        stop = true;
+                        break;
+                    }
                 }
                 tc::fence_after_sync();
                 const uint32_t ta = tmem + lane_base + kFwdACol + 64 * as;
@@ -314,8 +316,7 @@ interact_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
                         tc::mma_tf32_ta(dt, ta + 32 + 8 * kk, bd, idesc, true);
                     }
                     issued = true;
-                    tc::mma_commit(&empty[slot]);
-                    tc::mma_commit(&aempty[as]);
+                    tc::mma_commit(&empty[slot]);  // frees the B slot and, kFwdAS items on, the A slot
                 }
                 if (!ok)
                     break;
@@ -1020,8 +1021,8 @@ int launch_interact_fwd_tc(const float *e0, int64_t e0s, const float *emb, int64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return 1;
     const int P = (int)num_pairs_of(F, mode & kInteractSelf);
-    const size_t fixed = 1024 + (size_t)128 * (Fb + 1) * 4 + (size_t)((P + 3) & ~3) * 2 + (2 * kFwdAS + 4) * 8;
-    int NS = 2;  // B slots (18 KB): as many as fit, up to 8
+    const size_t fixed = 1024 + (size_t)128 * (Fb + 1) * 4 + (size_t)((P + 3) & ~3) * 2 + (kFwdAS + 4) * 8;
+    int NS = kFwdAS + 1;  // B slots (18 KB): as many as fit, up to 8, more than the A slots
     while (NS < 8 && fixed + (size_t)(NS + 1) * (kFwdSlotBytes + 16) <= kMaxSmem)
         NS++;
     const size_t smem = fixed + (size_t)NS * (kFwdSlotBytes + 16);
