@@ -1,11 +1,16 @@
-// Pairwise dot-product interaction, forward and backward.
+// Pairwise dot-product interaction, forward and backward, on the CUDA cores
+// (fp32 FMAs), and the dispatch between the kernel families.
 //
 // Follows "Notes/DLRM" (vault-aram.pages.dev), section 3 "The Pairwise
 // Interaction Layer": one dot product per pair of the vectors
 // {e0, e_1 .. e_N}, self pairs optional, the terms concatenated with e0.
 //
-// Forward design (operands the bulk tensor copy cannot describe; the usual
-// path is interact_tma.cu, same arithmetic): a CTA takes S samples.  The F x d
+// Dispatch: the tensor-core kernels (interact_tc.cu) where they apply, else
+// for the forward the bulk-tensor-copy kernel (interact_tma.cu) where the
+// copy engine can describe the operands, else the kernels below; all compute
+// the same values within the fp32 tolerance.
+//
+// Forward design (operands neither of the others takes): a CTA takes S samples.  The F x d
 // block Z of each sample
 // (row 0 = e0, rows 1..N = pooled embeddings) is staged through shared memory
 // in chunks of KC = 32 columns: each row chunk is one coalesced 128-byte read

@@ -1,4 +1,6 @@
-// Interaction forward fed by the tensor memory accelerator.
+// Interaction forward on the CUDA cores, fed by the tensor memory accelerator
+// (taken where the tensor-core kernel of interact_tc.cu does not apply, e.g.
+// d < 32 or more than 128 vectors per sample).
 //
 // Same arithmetic as interact_fwd_kernel ("Notes/DLRM", vault-aram.pages.dev,
 // section 3: one dot product per pair of {e0, e_1 .. e_N}, concatenated with
