@@ -48,8 +48,8 @@ METRIC = "emb-bag+interaction fwd/bwd/SGD samples/s; gathered GB/s as % of HBM p
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=250)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="multi-hot", choices=sorted(W.CONFIG_IDS))
     p.add_argument("--seed", type=int, default=0)
@@ -63,6 +63,12 @@ def parse_args():
                    help="row-wise update of the touched rows (adagrad: one fp32 accumulator per row)")
     p.add_argument("--fwd", choices=["separate", "fused"], default="separate",
                    help="fused: one kernel for the lookup and the interaction forward")
+    p.add_argument("--update", choices=["sorted", "atomic"], default="sorted",
+                   help="atomic: the SGD update by atomic reductions without coalescing (fp32 tables)")
+    p.add_argument("--targets", choices=["auto", "on", "off"], default="auto",
+                   help="also measure the capacity and uniform multi-hot workloads stage by stage "
+                        "(auto: with the default workload on one GPU)")
+    p.add_argument("--target-steps", type=int, default=40)
     p.add_argument("--batch", type=int, default=None, help="override the batch size (profiling runs)")
     p.add_argument("--tables", type=int, default=None, help="override the table count (profiling runs)")
     p.add_argument("--rows", type=int, default=None, help="override the rows per table (profiling runs)")
@@ -147,17 +153,51 @@ def calibrate_oracle(cfg, offsets, indices, seed, seconds, optimizer="sgd"):
     return int(max(probe, min(cfg["B"], seconds / max(per_sample, 1e-9))))
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), or the platform's description."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(cfg, offsets, indices, seed, seconds, optimizer="sgd"):
+    """The oracle timed on the host: the serial build (the parity oracle) on
+    one core, then its OpenMP build (the same loops, identical results) on all
+    cores, each on a sample sized for about `seconds`."""
     import oracle
     oracle.build()
+    oracle.use_openmp(False)
     Bs = calibrate_oracle(cfg, offsets, indices, seed, seconds, optimizer)
     s = oracle_sample(cfg, offsets, indices, Bs, seed)
     t0 = time.perf_counter()
     oracle_step(s, optimizer)
     el = time.perf_counter() - t0
-    return {"value": Bs / el, "unit": "samples/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {Bs} of {cfg['B']} samples of the same batch (all {cfg['T']} tables, "
-                      f"{s['indices'].size} lookups), full step in fp64 on one host core, {el:.1f} s"}
+    out = {"value": Bs / el, "unit": "samples/s", "cores": 1, "kind": "oracle",
+           "sample": f"first {Bs} of {cfg['B']} samples of the same batch (all {cfg['T']} tables, "
+                     f"{s['indices'].size} lookups), full step in fp64 on one host core, {el:.1f} s",
+           "cpu_model": cpu_model(), "host_cores": os.cpu_count()}
+    if oracle.use_openmp(True):
+        try:
+            Ba = calibrate_oracle(cfg, offsets, indices, seed, seconds, optimizer)
+            sa = oracle_sample(cfg, offsets, indices, Ba, seed)
+            t0 = time.perf_counter()
+            oracle_step(sa, optimizer)
+            ela = time.perf_counter() - t0
+            out["all_cores"] = {"value": Ba / ela, "unit": "samples/s", "cores": os.cpu_count(),
+                                "kind": "oracle, OpenMP build",
+                                "sample": f"first {Ba} of {cfg['B']} samples ({sa['indices'].size} lookups), "
+                                          f"{ela:.1f} s on all {os.cpu_count()} host cores"}
+        finally:
+            oracle.use_openmp(False)
+    else:
+        out["all_cores"] = None
+    return out
 
 
 def run_reference(args):
@@ -275,7 +315,7 @@ ADAGRAD_EPS = 1e-8
 class Step:
     """Device buffers and the launches of one step of the path."""
 
-    def __init__(self, cfg, seed, dev, schedule="overlap", fwd="separate", optimizer="sgd"):
+    def __init__(self, cfg, seed, dev, schedule="overlap", fwd="separate", optimizer="sgd", update="sorted"):
         import torch
 
         import sparse_dense_interaction_gb300 as sdi
@@ -297,8 +337,13 @@ class Step:
             self.de0 = torch.empty((B, d), device=dev)
         else:
             self.dpooled.copy_(torch.from_numpy(W.make_dpooled(cfg, seed)))
-        self.ws = torch.empty(sdi.dlrm_emb_bag_bwd_workspace_size(T, B, self.nnz, d), dtype=torch.uint8,
-                              device=dev)
+        self.update = update
+        if update == "atomic":
+            if cfg["dtype"] != "f32" or cfg["update"] != "sgd" or optimizer != "sgd":
+                raise ValueError("the atomic update serves fp32 tables with plain SGD")
+            schedule = "serial"  # nothing to coalesce ahead of the forward
+        self.ws = torch.empty(sdi.dlrm_emb_bag_bwd_workspace_size(T, B, self.nnz, d) if update == "sorted" else 0,
+                              dtype=torch.uint8, device=dev)
         self.grad = torch.empty((self.nnz, d), device=dev) if cfg["update"] == "grad" else None
         self.flag = torch.zeros(1, dtype=torch.int32, device=dev)
         self.schedule, self.fwd, self.optimizer = schedule, fwd, optimizer
@@ -343,7 +388,10 @@ class Step:
         if self.inter:
             call("interact_bwd", lambda: sdi.dlrm_interact_bwd(
                 self.e0, self.pooled, c["include_self"], self.dy, self.de0, self.dpooled), main)
-        if self.schedule == "overlap":
+        if self.update == "atomic":
+            call("emb_bag_bwd_atomic", lambda: sdi.dlrm_emb_bag_bwd_sgd_atomic(
+                self.tables, self.offsets, self.indices, c["B"], self.dpooled, c["lr"], err_flag=self.flag), main)
+        elif self.schedule == "overlap":
             main.wait_event(self.coalesced)
             if self.state is None:
                 call("reduce_sgd", lambda: sdi.dlrm_emb_bag_reduce_sgd(
@@ -455,9 +503,85 @@ def algorithmic_bytes(cfg, st):
     # the reduce + update kernel: sorted keys and positions, bag ids, the
     # pooled gradient, and one read-modify-write of every unique row
     out["seg_reduce"] = st.nnz * 12 + nb * d * 4 + 2 * uniq * d * es
+    # the whole backward (coalescing + reduce, or the atomic update): the
+    # indices and offsets, the pooled gradient, one read-modify-write of every
+    # unique row (the sort's own passes are not compulsory traffic)
+    out["backward"] = st.nnz * 8 + (nb + 1) * 8 + nb * d * 4 + 2 * uniq * d * es
+    out["emb_bag_bwd_atomic"] = out["backward"]
     if st.state is not None:  # AdaGrad: read-modify-write of each touched row's accumulator
         out["seg_reduce"] += 2 * uniq * 4
+        out["backward"] += 2 * uniq * 4
     return out, uniq
+
+
+def stage_times(kernel_ms, passes):
+    """Per-stage milliseconds of one step from the per-kernel times."""
+    coal = sum(kernel_ms.get(k, 0.0) for k in coalesce_kernel_names(passes))
+    red = sum(kernel_ms.get(k, 0.0) for k in REDUCE_KERNELS)
+    out = {"lookup": kernel_ms.get("emb_bag_fwd"), "coalesce": coal or None, "reduce": red or None}
+    if "emb_bag_bwd_atomic" in kernel_ms:
+        out["backward"] = kernel_ms["emb_bag_bwd_atomic"]
+    elif coal and red:
+        out["backward"] = coal + red
+    return out
+
+
+def measure_target(name, args, dev, update="sorted"):
+    """One workload measured stage by stage (serial schedule, kernel events):
+    the lookup, the coalescing, the reduce and the whole backward, each with
+    its algorithmic bytes and its fraction of the measured HBM peak."""
+    import torch
+
+    import sparse_dense_interaction_gb300 as sdi
+    cfg = W.make_config(name)
+    st = Step(cfg, args.seed, dev, "serial", "separate", "sgd", update)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        st.run()
+    torch.cuda.synchronize()
+    if sdi.dlrm_read_error(st.flag) != 0:
+        raise RuntimeError(f"device error flag in the {name} target")
+    K = args.target_steps
+    prof = KernelProfiler(torch, sdi, stream, K)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        st.run(prof)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_step = a.elapsed_time(b) / K
+    passes = (max(1, int(np.ceil(np.log2(max(cfg["rows"]))))) + 7) // 8
+    kernel_ms = {kernel_name(c, k, passes): float(np.mean(v)) for (c, k), v in prof.per_kernel_ms().items()}
+    alg, uniq = algorithmic_bytes(cfg, st)
+    peak, _ = measured_peaks()
+    stages = {}
+    for stage, ms in stage_times(kernel_ms, passes).items():
+        if ms is None:
+            continue
+        nbytes = {"lookup": alg["emb_bag_fwd"], "reduce": alg["seg_reduce"], "backward": alg["backward"]}.get(stage)
+        e = {"ms": ms}
+        if nbytes is not None:
+            gbs = nbytes / (ms / 1e3) / 1e9
+            e.update(bytes=nbytes, gbs=gbs, frac=gbs / peak)
+        stages[stage] = e
+    out = {"config": config_of(cfg), "update": update, "ms_per_step": ms_step,
+           "samples_per_s": cfg["B"] / (ms_step / 1e3), "steps": K, "unique_rows": uniq, "lookups": st.nnz,
+           "stages": stages}
+    del st, prof
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_targets(args, dev):
+    """The workloads the >= 70 % of HBM goal is set on: capacity (uniform
+    indices over 131 GB of fp32 tables) with both update paths, and the
+    multi-hot shapes with uniform indices."""
+    out = {}
+    for key, name, update in (("capacity", "capacity", "sorted"), ("capacity_atomic", "capacity", "atomic"),
+                              ("multi_hot_uniform", "multi-hot-uniform", "sorted")):
+        out[key] = measure_target(name, args, dev, update)
+    return out
 
 
 def run_ours(args):
@@ -481,7 +605,7 @@ def run_ours(args):
     sdi.load()
 
     cfg = workload_config(args)
-    st = Step(cfg, args.seed + rank, dev, args.schedule, args.fwd, args.optimizer)
+    st = Step(cfg, args.seed + rank, dev, args.schedule, args.fwd, args.optimizer, args.update)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         st.run()
@@ -550,21 +674,32 @@ def run_ours(args):
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base = cpu_baseline(cfg, st.offsets_h, st.indices_h, args.seed, args.cpu_seconds, args.optimizer)
+    gathered_bytes, unique_rows, lookups = st.nnz * cfg["d"] * es, uniq, st.nnz
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    targets = None
+    if world == 1 and (args.targets == "on" or (args.targets == "auto" and args.workload == "multi-hot"
+                                                  and args.batch is None and args.tables is None
+                                                  and args.rows is None)):
+        targets = run_targets(args, dev)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 accumulate, " + cfg["dtype"] + " tables",
             "data": "synthetic (seeded; Zipf/uniform indices, counter-hash tables)",
-            "config": dict(config_of(cfg), schedule=args.schedule, forward=args.fwd, optimizer=args.optimizer),
+            "config": dict(config_of(cfg), schedule=args.schedule, forward=args.fwd, optimizer=args.optimizer,
+                           update=args.update),
             "gathered": {"gbs": gathered, "frac_of_hbm_peak": gathered / peak,
-                         "bytes": st.nnz * cfg["d"] * es, "unique_rows": uniq, "lookups": st.nnz},
+                         "bytes": gathered_bytes, "unique_rows": unique_rows, "lookups": lookups},
             "roofline": roofline,
             "kernels_ms": kernel_ms,
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk,
             "cpu_baseline": base,
+            "targets": targets,
         }
         print(json.dumps(line))
     if world > 1:

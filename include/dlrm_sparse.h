@@ -95,8 +95,9 @@ int dlrm_emb_bag_fwd(const void *const *tables, const int64_t *rows, int T, int 
 /*
  * Row-wise int4 tables (DLRM_INT4).  The factlen.com page ("Terabyte Embedding
  * Tables and Compute-Bound Neural Layers Force Meta's DLRM to Split
- * Training", section "The limits of scale") reports 4-bit integer
- * quantization of the vectors; the format here is the row-wise affine codec.
+ * Training", section "Scaling limits and the reality of production") reports
+ * 4-bit integer quantization of the vectors; the format here is the row-wise
+ * affine codec.
  * A row of d values (d % 8 == 0, d <= 512) takes dlrm_int4_row_bytes(d)
  * bytes: d codes q of 4 bits (element 2j in the low nibble of byte j, 2j+1 in
  * the high nibble), then the row's fp32 scale s and fp32 bias b, then zero
@@ -297,6 +298,40 @@ int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d,
                          dlrm_stream_t stream);
 
 /*
+ * Embedding-bag backward with row-wise SGD applied by atomic reductions, for
+ * fp32 tables ("Notes/DLRM", section 5: the tables are trained by an
+ * optimizer; the same plain SGD on the touched rows as dlrm_emb_bag_bwd_sgd,
+ * without coalescing the duplicate lookups first):
+ *
+ *   tables[t][r] += -lr * dpooled[b][t]   for every lookup of row r in bag (t, b)
+ *
+ * Each bag's pooled gradient is read once; lookups of one row within a group
+ * of a bag's indices are merged, and every (bag, row) pair adds its share to
+ * the row with fp32 vector reductions performed in L2.  No sort, no
+ * workspace, no coalesced gradient (no grad_rows, no view).
+ *  - dtype must be DLRM_F32 (DLRM_ERR_UNSUPPORTED otherwise): a half-precision
+ *    table would be rounded at every reduction.
+ *  - A row touched by k bags receives k fp32 additions in an unspecified
+ *    order: the result is not reproducible bit for bit from run to run, and
+ *    its rounding error grows with k (about k * 2^-24 of |w| + |lr| * sum |g|
+ *    at worst), against one rounding in dlrm_emb_bag_bwd_sgd.  It suits index
+ *    streams spread over large tables (few lookups per row, as uniform
+ *    indices over tables much larger than the batch's lookups); skewed
+ *    streams, whose hot rows collect thousands of additions, are better served
+ *    by dlrm_emb_bag_bwd_sgd.  The reductions flush subnormal values to zero.
+ *  - lr == 0 or B == 0: nothing is launched.  Errors are flagged as in
+ *    dlrm_emb_bag_fwd (an out-of-range lookup is skipped; a bag with bad
+ *    offsets adds nothing); arguments otherwise as in dlrm_emb_bag_bwd_sgd.
+ * The vectorised path needs d % 4 == 0, 16-byte aligned tables and dpooled,
+ * and dpooled strides that are multiples of 4; other layouts take a scalar
+ * path.
+ */
+int dlrm_emb_bag_bwd_sgd_atomic(void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                                const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                                const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride,
+                                float lr, int32_t *err_flag, dlrm_stream_t stream);
+
+/*
  * The two halves of dlrm_emb_bag_bwd_sgd, for callers that overlap them with
  * other work.  dlrm_emb_bag_coalesce does the coalescing (the stable sort by
  * (table, row) and the run-length encoding) into the workspace; it reads only
@@ -366,12 +401,18 @@ int dlrm_emb_bag_reduce_adagrad(void *const *tables, float *const *state, const 
  * and allocates nothing: its scratch is a fixed array of
  * DLRM_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library holds until the process exits.
- *  - Sizes whose scratch would not fit (dlrm_emb_bag_bwd_workspace_size(T, B,
+ *  - The status of every refused call is the one dlrm_emb_bag_bwd_sgd returns
+ *    for the same arguments and a workspace of DLRM_NOALLOC_SCRATCH_BYTES:
+ *    sizes whose scratch would not fit (dlrm_emb_bag_bwd_workspace_size(T, B,
  *    nnz, d) > DLRM_NOALLOC_SCRATCH_BYTES; about 1.7M lookups at d = 128) are
- *    refused with DLRM_ERR_WORKSPACE_TOO_SMALL before anything is launched.
- *  - The first call on each device looks up the array's device address (a
- *    CUDA runtime query, made with that device current); make that first call
- *    before any stream capture.
+ *    refused with DLRM_ERR_WORKSPACE_TOO_SMALL, before the device is touched.
+ *  - Each call looks up the array's device address (a CUDA runtime query,
+ *    made with the calling device current).  With lazily loaded modules (the
+ *    CUDA default) the first call on a device is the one that loads the
+ *    module and makes the array resident there, so it can fail with
+ *    DLRM_ERR_CUDA when the device has no memory left.  A service that must
+ *    not claim device memory once it runs should make one small call at
+ *    start-up (nnz = 0 is enough) and before any stream capture.
  *  - All calls share the array and it keeps the last call's contents; the
  *    call re-initialises what it needs.  Calls that may run at the same time
  *    on the GPU (different streams with no ordering between them) race on it

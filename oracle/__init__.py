@@ -28,6 +28,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "dlrm_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "_build", "liboracle_omp.so")
 
 F32, F16, BF16, INT4 = 0, 1, 2, 3
 _DTYPE_CODES = {"f32": F32, "f16": F16, "bf16": BF16, "int4": INT4}
@@ -36,6 +37,7 @@ OK, INVALID_ARG, INDEX_OOB, BAD_OFFSETS, NO_MEMORY = 0, -1, -4, -5, -8
 
 _lock = threading.Lock()
 _lib = None
+_variant = _LIB
 
 
 class OracleError(RuntimeError):
@@ -44,25 +46,53 @@ class OracleError(RuntimeError):
         self.status = status
 
 
+def _compile(target, extra):
+    tmp = target + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-Wall", "-Wextra",
+                    "-Wno-unknown-pragmas"] + extra + ["-shared", "-fPIC", _SRC, "-o", tmp, "-lm"],
+                   check=True, capture_output=True)
+    os.replace(tmp, target)
+
+
 def build(force: bool = False) -> str:
-    """Compiles the oracle with gcc into ``oracle/_build/liboracle.so``."""
+    """Compiles the oracle with gcc into ``oracle/_build/liboracle.so``, and
+    (best effort) its OpenMP build ``liboracle_omp.so``, used only to time the
+    oracle on all host cores."""
     os.makedirs(os.path.dirname(_LIB), exist_ok=True)
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
-    tmp = _LIB + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-                    "-Wall", "-Wextra", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"],
-                   check=True)
-    os.replace(tmp, _LIB)
+    for target, extra, required in ((_LIB, [], True), (_LIB_OMP, ["-fopenmp"], False)):
+        if not force and os.path.exists(target) and os.path.getmtime(target) >= os.path.getmtime(_SRC):
+            continue
+        try:
+            _compile(target, extra)
+        except (subprocess.CalledProcessError, OSError):
+            if required:
+                raise
     return _LIB
+
+
+def use_openmp(flag: bool) -> bool:
+    """Switches the loaded library between the serial build (the parity
+    oracle) and the OpenMP build (the same loops on all host cores; identical
+    results).  Returns whether the requested build is in use."""
+    global _lib, _variant
+    want = _LIB_OMP if flag else _LIB
+    build()
+    if flag and not os.path.exists(_LIB_OMP):
+        return False
+    with _lock:
+        if _variant != want:
+            _lib = None
+            _variant = want
+    _load()
+    return True
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            build()
+            lib = ctypes.CDLL(_variant)
             i64, i32, vp, dp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
             lib.oracle_decode.argtypes = [i32, vp, i64, dp]
             lib.oracle_emb_bag_fwd.argtypes = [i32, i32, i32, vp, vp, i64, vp, vp, i64, dp, dp]
@@ -189,6 +219,9 @@ def interact_bwd(e0, emb, dy, include_self: bool, e0_mag=None, emb_mag=None, dy_
     """Gradients of the interaction: returns (de0, de0_mag, demb, demb_mag)."""
     e0, emb, dy = _f64(e0), _f64(emb), _f64(dy)
     B, N, d = emb.shape
+    width = d * (N + 1 if alongside else 1) + num_pairs(N, include_self)
+    if dy.shape != (B, width) or e0.shape != (B, d):
+        raise ValueError(f"interact_bwd: dy must be [{B}][{width}] and e0 [{B}][{d}]")
     de0 = np.empty((B, d), dtype=np.float64)
     de0m = np.empty_like(de0)
     demb = np.empty((B, N, d), dtype=np.float64)

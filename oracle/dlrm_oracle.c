@@ -33,7 +33,11 @@
  * the readings used are stated at each function.
  *
  * Build: gcc -O2 -ffp-contract=off -shared -fPIC (no fused multiply-add, so
- * results are identical on x86-64 and AArch64 hosts).
+ * results are identical on x86-64 and AArch64 hosts).  The same source built
+ * with -fopenmp spreads the outer loops (tables and samples, samples, unique
+ * keys) over the host's cores; every output element is still computed by one
+ * thread in the order written here, so both builds give identical results.
+ * The parallel build exists only to time the oracle on all cores.
  */
 #include <math.h>
 #include <stdint.h>
@@ -76,8 +80,8 @@ static double decode_bfloat16(uint16_t h)
 
 /*
  * Row-wise 4-bit tables.  The factlen.com page ("...Force Meta's DLRM to Split
- * Training", section "The limits of scale") reports 4-bit integer
- * quantization of the vectors without a format; the reading here is the
+ * Training", section "Scaling limits and the reality of production") reports
+ * 4-bit integer quantization of the vectors without a format; the reading here is the
  * common row-wise affine codec: each row stores d 4-bit codes q (element 2j
  * in the low nibble of byte j, element 2j+1 in the high nibble), then its
  * fp32 scale s and fp32 bias b; the row is padded to a multiple of 16 bytes.
@@ -176,6 +180,11 @@ int oracle_emb_bag_fwd(int T, int d, int dtype, const void *const *tables, const
     int st = check_offsets(T, B, offsets, nnz);
     if (st != ORACLE_OK)
         return st;
+    for (int t = 0; t < T; t++)
+        for (int64_t k = offsets[(int64_t)t * B]; k < offsets[(int64_t)(t + 1) * B]; k++)
+            if (indices[k] < 0 || indices[k] >= rows[t])
+                return ORACLE_INDEX_OOB;
+#pragma omp parallel for collapse(2) schedule(dynamic, 64)
     for (int t = 0; t < T; t++) {
         for (int64_t b = 0; b < B; b++) {
             double *out = pooled + (b * T + t) * (int64_t)d;
@@ -186,8 +195,6 @@ int oracle_emb_bag_fwd(int T, int d, int dtype, const void *const *tables, const
             }
             for (int64_t k = offsets[(int64_t)t * B + b]; k < offsets[(int64_t)t * B + b + 1]; k++) {
                 int64_t r = indices[k];
-                if (r < 0 || r >= rows[t])
-                    return ORACLE_INDEX_OOB;
                 for (int e = 0; e < d; e++) {
                     out[e] += table_element(tables[t], dtype, d, r * d + e);
                     mag[e] += table_element_mag(tables[t], dtype, d, r * d + e);
@@ -239,6 +246,7 @@ int oracle_interact_fwd(int N, int d, int64_t B, int mode,
     int F = N + 1;
     int include_self = mode & 1;
     int64_t width = interact_width(N, d, mode);
+#pragma omp parallel for schedule(dynamic, 16)
     for (int64_t b = 0; b < B; b++) {
         double *yr = y + b * width;
         double *ym = y_mag + b * width;
@@ -297,61 +305,68 @@ int oracle_interact_bwd(int N, int d, int64_t B, int mode,
     int F = N + 1;
     int include_self = mode & 1;
     int64_t width = interact_width(N, d, mode);
-    double *dz = (double *)calloc((size_t)F * d, sizeof(double));
-    double *dzm = (double *)calloc((size_t)F * d, sizeof(double));
-    if (!dz || !dzm) {
-        free(dz);
-        free(dzm);
-        return ORACLE_NO_MEMORY;
-    }
-    for (int64_t b = 0; b < B; b++) {
-        memset(dz, 0, sizeof(double) * (size_t)F * d);
-        memset(dzm, 0, sizeof(double) * (size_t)F * d);
-        int64_t p = (mode & 2) ? (int64_t)F * d : d;
-        for (int i = 0; i < F; i++) {
-            int jmax = include_self ? i : i - 1;
-            for (int j = 0; j <= jmax; j++) {
-                double g = dy[b * width + p];
-                double gm = mag_or_abs(dy_mag, dy, b * width + p);
-                p++;
-                for (int e = 0; e < d; e++) {
-                    int64_t ii = (i == 0) ? b * d + e : (b * N + (i - 1)) * (int64_t)d + e;
-                    int64_t jj = (j == 0) ? b * d + e : (b * N + (j - 1)) * (int64_t)d + e;
-                    double zi = (i == 0) ? e0[ii] : emb[ii];
-                    double zj = (j == 0) ? e0[jj] : emb[jj];
-                    double mi = (i == 0) ? mag_or_abs(e0_mag, e0, ii) : mag_or_abs(emb_mag, emb, ii);
-                    double mj = (j == 0) ? mag_or_abs(e0_mag, e0, jj) : mag_or_abs(emb_mag, emb, jj);
-                    if (i == j) {
-                        dz[(int64_t)i * d + e] += 2.0 * g * zi;
-                        dzm[(int64_t)i * d + e] += 2.0 * gm * mi;
-                    } else {
-                        dz[(int64_t)i * d + e] += g * zj;
-                        dzm[(int64_t)i * d + e] += gm * mj;
-                        dz[(int64_t)j * d + e] += g * zi;
-                        dzm[(int64_t)j * d + e] += gm * mi;
+    int failed = 0;
+    /* one scratch pair per thread (a single one in the serial build) */
+#pragma omp parallel
+    {
+        double *dz = (double *)calloc((size_t)F * d, sizeof(double));
+        double *dzm = (double *)calloc((size_t)F * d, sizeof(double));
+        if (!dz || !dzm) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t b = 0; b < B; b++) {
+            if (!dz || !dzm)
+                continue;
+            memset(dz, 0, sizeof(double) * (size_t)F * d);
+            memset(dzm, 0, sizeof(double) * (size_t)F * d);
+            int64_t p = (mode & 2) ? (int64_t)F * d : d;
+            for (int i = 0; i < F; i++) {
+                int jmax = include_self ? i : i - 1;
+                for (int j = 0; j <= jmax; j++) {
+                    double g = dy[b * width + p];
+                    double gm = mag_or_abs(dy_mag, dy, b * width + p);
+                    p++;
+                    for (int e = 0; e < d; e++) {
+                        int64_t ii = (i == 0) ? b * d + e : (b * N + (i - 1)) * (int64_t)d + e;
+                        int64_t jj = (j == 0) ? b * d + e : (b * N + (j - 1)) * (int64_t)d + e;
+                        double zi = (i == 0) ? e0[ii] : emb[ii];
+                        double zj = (j == 0) ? e0[jj] : emb[jj];
+                        double mi = (i == 0) ? mag_or_abs(e0_mag, e0, ii) : mag_or_abs(emb_mag, emb, ii);
+                        double mj = (j == 0) ? mag_or_abs(e0_mag, e0, jj) : mag_or_abs(emb_mag, emb, jj);
+                        if (i == j) {
+                            dz[(int64_t)i * d + e] += 2.0 * g * zi;
+                            dzm[(int64_t)i * d + e] += 2.0 * gm * mi;
+                        } else {
+                            dz[(int64_t)i * d + e] += g * zj;
+                            dzm[(int64_t)i * d + e] += gm * mj;
+                            dz[(int64_t)j * d + e] += g * zi;
+                            dzm[(int64_t)j * d + e] += gm * mi;
+                        }
                     }
                 }
             }
-        }
-        for (int e = 0; e < d; e++) {
-            de0[b * d + e] = dy[b * width + e] + dz[e];
-            de0_mag[b * d + e] = mag_or_abs(dy_mag, dy, b * width + e) + dzm[e];
-        }
-        for (int i = 1; i < F; i++)
             for (int e = 0; e < d; e++) {
-                /* with the embeddings alongside, each also receives the gradient of its copy */
-                double cp = 0.0, cpm = 0.0;
-                if (mode & 2) {
-                    cp = dy[b * width + (int64_t)i * d + e];
-                    cpm = mag_or_abs(dy_mag, dy, b * width + (int64_t)i * d + e);
-                }
-                demb[(b * N + (i - 1)) * (int64_t)d + e] = cp + dz[(int64_t)i * d + e];
-                demb_mag[(b * N + (i - 1)) * (int64_t)d + e] = cpm + dzm[(int64_t)i * d + e];
+                de0[b * d + e] = dy[b * width + e] + dz[e];
+                de0_mag[b * d + e] = mag_or_abs(dy_mag, dy, b * width + e) + dzm[e];
             }
+            for (int i = 1; i < F; i++)
+                for (int e = 0; e < d; e++) {
+                    /* with the embeddings alongside, each also receives the gradient of its copy */
+                    double cp = 0.0, cpm = 0.0;
+                    if (mode & 2) {
+                        cp = dy[b * width + (int64_t)i * d + e];
+                        cpm = mag_or_abs(dy_mag, dy, b * width + (int64_t)i * d + e);
+                    }
+                    demb[(b * N + (i - 1)) * (int64_t)d + e] = cp + dz[(int64_t)i * d + e];
+                    demb_mag[(b * N + (i - 1)) * (int64_t)d + e] = cpm + dzm[(int64_t)i * d + e];
+                }
+        }
+        free(dz);
+        free(dzm);
     }
-    free(dz);
-    free(dzm);
-    return ORACLE_OK;
+    return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
 
 /* One lookup, keyed by (table, row) and tagged with its position. */
@@ -454,13 +469,15 @@ int oracle_sgd(int T, int d, int dtype, const void *const *tables, const int64_t
         for (int64_t b = 0; b < B; b++)
             for (int64_t k = offsets[(int64_t)t * B + b]; k < offsets[(int64_t)t * B + b + 1]; k++)
                 bag_of[k] = b;
-    for (int64_t u = 0; u < U; u++) {
-        int t = uniq_table[u];
-        int64_t r = uniq_row[u];
-        if (t < 0 || t >= T || r < 0 || r >= rows[t]) {
+    for (int64_t u = 0; u < U; u++)
+        if (uniq_table[u] < 0 || uniq_table[u] >= T || uniq_row[u] < 0 || uniq_row[u] >= rows[uniq_table[u]]) {
             free(bag_of);
             return ORACLE_INDEX_OOB;
         }
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t u = 0; u < U; u++) {
+        int t = uniq_table[u];
+        int64_t r = uniq_row[u];
         for (int e = 0; e < d; e++) {
             double g = 0.0, gm = 0.0;
             for (int64_t j = seg_off[u]; j < seg_off[u + 1]; j++) {
@@ -518,6 +535,7 @@ int oracle_adagrad(int T, int d, int dtype, const void *const *tables, const int
                         uniq_table, uniq_row, seg_off, U, grad, grad_mag, new_row, new_row_mag);
     if (st != ORACLE_OK)
         return st;
+#pragma omp parallel for schedule(dynamic, 64)
     for (int64_t u = 0; u < U; u++) {
         const int t = uniq_table[u];
         const int64_t r = uniq_row[u];

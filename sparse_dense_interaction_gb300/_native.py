@@ -48,6 +48,8 @@ SIGNATURES = {
     "dlrm_emb_bag_bwd_sgd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64,
                                     _i64, _f32, _vp, _i64, _vp, _sz, ctypes.POINTER(CoalescedView),
                                     _vp, _vp]),
+    "dlrm_emb_bag_bwd_sgd_atomic": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64,
+                                           _i64, _f32, _vp, _vp]),
     "dlrm_emb_bag_bwd_sgd_noalloc": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp,
                                             _i64, _i64, _f32, _vp, _i64, ctypes.POINTER(CoalescedView),
                                             _vp, _vp]),
@@ -353,24 +355,61 @@ def dlrm_emb_bag_reduce_adagrad(tables, state, nnz: int, B: int, dpooled, lr: fl
                                               _stream(stream)), "dlrm_emb_bag_reduce_adagrad")
 
 
+def dlrm_emb_bag_bwd_sgd_atomic(tables, offsets, indices, B: int, dpooled, lr: float, err_flag=None,
+                                stream=None):
+    """Row-wise SGD on fp32 ``tables`` in place by atomic reductions, without
+    coalescing the duplicate lookups (no workspace, no coalesced gradient).
+    The summation order of a row touched by several bags is unspecified."""
+    ptrs, rows, T, d, dtype = _tables(tables)
+    if dpooled.stride(2) != 1:
+        raise ValueError("dpooled must have unit stride in its last dimension")
+    _check(load().dlrm_emb_bag_bwd_sgd_atomic(ptrs, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices),
+                                              indices.numel(), B, dpooled.data_ptr(), dpooled.stride(0),
+                                              dpooled.stride(1), float(lr), _ptr(err_flag), _stream(stream)),
+           "dlrm_emb_bag_bwd_sgd_atomic")
+
+
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
+class _DeviceArray:
+    """A device pointer the library owns, described for torch.as_tensor (CUDA array interface)."""
+
+    def __init__(self, ptr, n, typestr):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
+def _raw_view_tensors(view, nnz):
+    def sub(ptr, n, typestr):
+        return torch.as_tensor(_DeviceArray(ptr, n, typestr), device="cuda")
+
+    return dict(sorted_pos=sub(view.sorted_pos, nnz, "<i4"), sorted_row=sub(view.sorted_row, nnz, "<i4"),
+                uniq_table=sub(view.uniq_table, nnz, "<i4"), uniq_row=sub(view.uniq_row, nnz, "<i4"),
+                seg_off=sub(view.seg_off, nnz + 1, "<i4"), num_unique=sub(view.num_unique, 1, "<i8"))
+
+
 def dlrm_emb_bag_bwd_sgd_noalloc(tables, offsets, indices, B: int, dpooled, lr: float,
-                                 grad_rows=None, err_flag=None, stream=None):
+                                 grad_rows=None, err_flag=None, stream=None, want_view: bool = False):
     """:func:`dlrm_emb_bag_bwd_sgd` without a workspace: the library's fixed
     scratch array is used instead, so nothing is allocated.  For callers that
     cannot allocate device memory; sizes whose scratch exceeds
-    ``NOALLOC_SCRATCH_BYTES`` raise (status DLRM_ERR_WORKSPACE_TOO_SMALL)."""
+    ``NOALLOC_SCRATCH_BYTES`` raise (status DLRM_ERR_WORKSPACE_TOO_SMALL).
+    With ``want_view`` returns tensors aliasing the coalescing results inside
+    that array (as :func:`dlrm_emb_bag_bwd_sgd`; valid until the next call)."""
     ptrs, rows, T, d, dtype = _tables(tables)
     if dpooled.stride(2) != 1:
         raise ValueError("dpooled must have unit stride in its last dimension")
     cap = 0 if grad_rows is None else grad_rows.shape[0]
+    view = CoalescedView()
+    nnz = indices.numel()
     _check(load().dlrm_emb_bag_bwd_sgd_noalloc(ptrs, rows, T, d, dtype, offsets.data_ptr(), _ptr(indices),
-                                               indices.numel(), B, dpooled.data_ptr(), dpooled.stride(0),
-                                               dpooled.stride(1), float(lr), _ptr(grad_rows), cap, None,
+                                               nnz, B, dpooled.data_ptr(), dpooled.stride(0),
+                                               dpooled.stride(1), float(lr), _ptr(grad_rows), cap,
+                                               ctypes.byref(view) if want_view else None,
                                                _ptr(err_flag), _stream(stream)),
            "dlrm_emb_bag_bwd_sgd_noalloc")
+    return _raw_view_tensors(view, nnz) if want_view else None
 
 
 def dlrm_read_error(err_flag, stream=None) -> int:

@@ -80,6 +80,8 @@ int launch_coalesce(const TableSet &, int, int, const int64_t *, const int64_t *
                     dlrm_coalesced_view *, int32_t *, cudaStream_t);
 int launch_reduce_sgd(const TableSet &, int, int, int, int64_t, int64_t, const float *, int64_t, int64_t, float,
                       float *, int64_t, void *, bool, int32_t *, cudaStream_t, float, float *const *);
+int launch_emb_bag_bwd_atomic(const TableSet &, int, int, const int64_t *, const int64_t *, int64_t, int64_t,
+                              const float *, int64_t, int64_t, float, bool, int32_t *, cudaStream_t);
 
 // Lookup positions are 32-bit in the backward's sort and scans; the bound
 // leaves headroom for tile and chunk arithmetic.
@@ -92,8 +94,7 @@ static const int kInt4MaxD = 512;  // 32 lanes of 16 codes
 static bool aligned(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
 // Common checks of the table arguments; fills the kernel-parameter view.
-static int make_tables(const void *const *tables, const int64_t *rows, int T, int d, int dtype,
-                       TableSet &ts)
+int make_tables(const void *const *tables, const int64_t *rows, int T, int d, int dtype, TableSet &ts)
 {
     if (!tables || !rows || T <= 0 || d <= 0)
         return DLRM_ERR_INVALID_ARG;
@@ -311,9 +312,13 @@ size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d)
     return emb_bag_bwd_workspace(T, nnz, d);
 }
 
+}  // extern "C"
+
+namespace dlrm {
+
 // Checks shared by the backward's calls: the sizes and the coalescing inputs.
-static int check_coalesce_args(int T, int d, const int64_t *offsets, const int64_t *indices, int64_t nnz,
-                               int64_t B, const void *workspace, size_t workspace_bytes)
+int check_coalesce_args(int T, int d, const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                        const void *workspace, size_t workspace_bytes)
 {
     if (B < 0 || nnz < 0)
         return DLRM_ERR_INVALID_ARG;
@@ -331,8 +336,8 @@ static int check_coalesce_args(int T, int d, const int64_t *offsets, const int64
 }
 
 // Checks of the reduce's inputs: pooled gradients, learning rate, outputs.
-static int check_reduce_args(int64_t nnz, const float *dpooled, int64_t dp_sample_stride,
-                             int64_t dp_table_stride, float lr, const float *grad_rows, int64_t grad_rows_cap)
+int check_reduce_args(int64_t nnz, const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride,
+                      float lr, const float *grad_rows, int64_t grad_rows_cap)
 {
     if (dp_sample_stride < 0 || dp_table_stride < 0 || grad_rows_cap < 0)
         return DLRM_ERR_INVALID_ARG;
@@ -347,6 +352,27 @@ static int check_reduce_args(int64_t nnz, const float *dpooled, int64_t dp_sampl
     return DLRM_OK;
 }
 
+// Every host check of dlrm_emb_bag_bwd_sgd, in its order; also used by the
+// call without a workspace (with its fixed scratch as the workspace).
+int check_bwd_sgd_args(void *const *tables, const int64_t *rows, int T, int d, int dtype, const int64_t *offsets,
+                       const int64_t *indices, int64_t nnz, int64_t B, const float *dpooled, int64_t dpss,
+                       int64_t dpts, float lr, const float *grad_rows, int64_t grad_rows_cap, const void *workspace,
+                       size_t workspace_bytes, TableSet &ts)
+{
+    int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
+    if (s != DLRM_OK)
+        return s;
+    if (dtype == DLRM_INT4)  // 4-bit tables are looked up, not trained
+        return DLRM_ERR_UNSUPPORTED;
+    if ((s = check_reduce_args(nnz, dpooled, dpss, dpts, lr, grad_rows, grad_rows_cap)) != DLRM_OK)
+        return s;
+    return check_coalesce_args(T, d, offsets, indices, nnz, B, workspace, workspace_bytes);
+}
+
+}  // namespace dlrm
+
+extern "C" {
+
 int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d, int dtype,
                          const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
                          const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride,
@@ -355,20 +381,40 @@ int dlrm_emb_bag_bwd_sgd(void *const *tables, const int64_t *rows, int T, int d,
                          dlrm_stream_t stream)
 {
     TableSet ts;
-    int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
+    const int s = check_bwd_sgd_args(tables, rows, T, d, dtype, offsets, indices, nnz, B, dpooled, dp_sample_stride,
+                                     dp_table_stride, lr, grad_rows, grad_rows_cap, workspace, workspace_bytes, ts);
     if (s != DLRM_OK)
-        return s;
-    if (dtype == DLRM_INT4)  // 4-bit tables are looked up, not trained
-        return DLRM_ERR_UNSUPPORTED;
-    if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, grad_rows, grad_rows_cap)) !=
-        DLRM_OK)
-        return s;
-    if ((s = check_coalesce_args(T, d, offsets, indices, nnz, B, workspace, workspace_bytes)) != DLRM_OK)
         return s;
     const bool vec = emb_bag_bwd_vectorisable(ts, T, d, dpooled, dp_sample_stride, dp_table_stride, grad_rows);
     return launch_emb_bag_bwd(ts, T, d, dtype, offsets, indices, nnz, B, dpooled, dp_sample_stride,
                               dp_table_stride, lr, grad_rows, grad_rows ? grad_rows_cap : 0, workspace, vec,
                               view, err_flag, static_cast<cudaStream_t>(stream));
+}
+
+int dlrm_emb_bag_bwd_sgd_atomic(void *const *tables, const int64_t *rows, int T, int d, int dtype,
+                                const int64_t *offsets, const int64_t *indices, int64_t nnz, int64_t B,
+                                const float *dpooled, int64_t dp_sample_stride, int64_t dp_table_stride,
+                                float lr, int32_t *err_flag, dlrm_stream_t stream)
+{
+    TableSet ts;
+    int s = make_tables(const_cast<const void *const *>(tables), rows, T, d, dtype, ts);
+    if (s != DLRM_OK)
+        return s;
+    if (dtype != DLRM_F32)  // one fp32 reduction per lookup: half tables would round at every one
+        return DLRM_ERR_UNSUPPORTED;
+    if ((s = check_reduce_args(nnz, dpooled, dp_sample_stride, dp_table_stride, lr, nullptr, 0)) != DLRM_OK)
+        return s;
+    if (B < 0 || nnz < 0 || (B == 0 && nnz != 0))
+        return DLRM_ERR_INVALID_ARG;
+    if (nnz > kMaxLookups || B > (int64_t)0x7fffffffLL)
+        return DLRM_ERR_UNSUPPORTED;
+    if (!offsets || !aligned(offsets, 8) || (nnz > 0 && (!indices || !aligned(indices, 8))))
+        return DLRM_ERR_INVALID_ARG;
+    if (B == 0 || lr == 0.f)
+        return DLRM_OK;
+    const bool vec = emb_bag_bwd_vectorisable(ts, T, d, dpooled, dp_sample_stride, dp_table_stride, nullptr);
+    return launch_emb_bag_bwd_atomic(ts, T, d, offsets, indices, nnz, B, dpooled, dp_sample_stride, dp_table_stride,
+                                     lr, vec, err_flag, static_cast<cudaStream_t>(stream));
 }
 
 int dlrm_emb_bag_coalesce(const int64_t *rows, int T, int d, const int64_t *offsets, const int64_t *indices,

@@ -33,6 +33,14 @@ int allow_dynamic_smem(const void *kernel, int bytes, std::atomic<unsigned long 
 // Whether the interaction calls may take the tensor-core kernels (the
 // process-wide setting of dlrm_set_interact_kernel).
 bool interact_tensor_cores();
+// Host checks shared by the entry points (api.cu): the table arguments (fills
+// the kernel-parameter view), and the whole argument list of the backward with
+// SGD (the call without a workspace passes its fixed scratch as workspace).
+int make_tables(const void *const *tables, const int64_t *rows, int T, int d, int dtype, TableSet &ts);
+int check_bwd_sgd_args(void *const *tables, const int64_t *rows, int T, int d, int dtype, const int64_t *offsets,
+                       const int64_t *indices, int64_t nnz, int64_t B, const float *dpooled, int64_t dpss,
+                       int64_t dpts, float lr, const float *grad_rows, int64_t grad_rows_cap, const void *workspace,
+                       size_t workspace_bytes, TableSet &ts);
 
 __device__ __forceinline__ void raise_flag(int32_t *flag, int bits)
 {

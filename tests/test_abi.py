@@ -175,3 +175,47 @@ def test_interaction_kernel_setting(lib):
 def test_read_error_needs_a_flag(lib):
     assert lib.dlrm_read_error(None, None) == _native.ERR_INVALID_ARG
     assert lib.dlrm_clear_error(None, None) == _native.ERR_INVALID_ARG
+
+
+def test_atomic_backward_rejects_bad_arguments(lib):
+    p, r = _tables(2)
+    call = lambda **kw: lib.dlrm_emb_bag_bwd_sgd_atomic(
+        p, r, 2, 16, kw.get("dtype", 0), kw.get("offsets", FAKE), FAKE, kw.get("nnz", 100), kw.get("B", 8),
+        kw.get("dp", FAKE), kw.get("dpss", 32), 16, kw.get("lr", 0.1), None, None)
+    assert call(dtype=_native.F16) == _native.ERR_UNSUPPORTED  # fp32 tables only
+    assert call(dtype=_native.BF16) == _native.ERR_UNSUPPORTED
+    assert call(dtype=_native.INT4) == _native.ERR_UNSUPPORTED
+    assert call(nnz=-1) == _native.ERR_INVALID_ARG
+    assert call(B=0) == _native.ERR_INVALID_ARG  # no bags cannot hold lookups
+    assert call(nnz=(1 << 31) + 1) == _native.ERR_UNSUPPORTED
+    assert call(lr=float("nan")) == _native.ERR_INVALID_ARG
+    assert call(offsets=None) == _native.ERR_INVALID_ARG
+    assert call(dp=None) == _native.ERR_INVALID_ARG
+    assert call(dpss=-1) == _native.ERR_INVALID_ARG
+    assert call(lr=0.0) == _native.OK  # nothing to update, nothing launched
+    assert call(B=0, nnz=0) == _native.OK
+    assert lib.dlrm_kernel_launch_count() == 0
+
+
+def test_noalloc_returns_the_workspace_calls_statuses(lib):
+    # the call without a workspace runs dlrm_emb_bag_bwd_sgd's own checks, its
+    # fixed array in place of the workspace: every refused call gets the same
+    # status (all of these fail on the host, before any device lookup)
+    p, r = _tables(2)
+    scratch = _native.NOALLOC_SCRATCH_BYTES
+    big = 1 << 21  # lookups whose scratch exceeds the array
+    assert sdi.dlrm_emb_bag_bwd_workspace_size(2, 8, big, 16) > scratch
+    cases = [dict(T=0), dict(d=0), dict(dtype=4), dict(dtype=_native.INT4), dict(dtype=_native.INT4, d=12),
+             dict(nnz=-1), dict(nnz=(1 << 31) + 1), dict(B=-1), dict(B=0), dict(lr=float("nan")),
+             dict(offsets=None), dict(dp=None), dict(dpss=-1), dict(dpss=(1 << 29) + 1), dict(cap=-1),
+             dict(nnz=big), dict(tables=None), dict(grad=FAKE + 2)]
+    for kw in cases:
+        kw.setdefault("tables", p)
+        args = lambda: (kw["tables"], r, kw.get("T", 2), kw.get("d", 16), kw.get("dtype", 0),
+                        kw.get("offsets", FAKE), FAKE, kw.get("nnz", 100), kw.get("B", 8), kw.get("dp", FAKE),
+                        kw.get("dpss", 32), 16, kw.get("lr", 0.1), kw.get("grad", None), kw.get("cap", 0))
+        want = lib.dlrm_emb_bag_bwd_sgd(*args(), 0x100000, scratch, None, None, None)
+        got = lib.dlrm_emb_bag_bwd_sgd_noalloc(*args(), None, None, None)
+        assert want != _native.OK, kw
+        assert got == want, (kw, got, want)
+    assert lib.dlrm_kernel_launch_count() == 0

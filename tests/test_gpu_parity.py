@@ -368,6 +368,62 @@ def test_long_runs_cross_chunks_and_tiles():
                  REL["f32"], "long-run rows")
 
 
+def _runs_of_lengths(rng, lengths, rows):
+    """Lookups of one table in which row r_i (distinct, increasing) appears
+    lengths[i] times, shuffled over the positions."""
+    rws = np.sort(rng.choice(rows, size=len(lengths), replace=False))
+    idx = np.repeat(rws, lengths)
+    rng.shuffle(idx)
+    return idx
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 128), ("f16", 128), ("bf16", 64), ("f32", 96), ("f16", 256),
+                                     ("f32", 16)])
+def test_runs_of_every_length_short_and_long(dtype, d):
+    # runs of 1 .. 9 lookups (the reduce takes runs of a few lookups that end
+    # inside a tile in a separate, run-parallel phase), a few hundred long
+    # runs, runs that end exactly at a tile's end or continue into the next
+    # tile, and a table of only length-1 runs spanning several tiles
+    rng = np.random.default_rng(17)
+    B = 2500
+    pattern = [1, 2, 3, 4, 5, 1, 1, 4, 4, 9, 1, 2, 3, 700, 1, 4, 2, 4100, 3, 1]
+    lengths0 = (pattern * 60)[:400]
+    idx0 = _runs_of_lengths(rng, lengths0, 200000)
+    idx1 = _runs_of_lengths(rng, [1] * 9000, 50000)
+    idx2 = _runs_of_lengths(rng, [4] * 1024 + [5] * 3 + [1] * 900, 9000)
+    per_table = [idx0, idx1, idx2]
+    offsets, indices = [0], []
+    for idx in per_table:
+        cuts = np.sort(rng.integers(0, idx.size + 1, B - 1))
+        bounds = np.concatenate([[0], cuts, [idx.size]])
+        for b in range(B):
+            indices.extend(idx[bounds[b]:bounds[b + 1]].tolist())
+            offsets.append(len(indices))
+    offsets = np.array(offsets, dtype=np.int64)
+    indices = np.array(indices, dtype=np.int64)
+    cfg = W.make_config("multi-hot", T=3, rows=[200000, 50000, 9000], B=B, d=d, dtype=dtype)
+    host = W.tables_host(cfg)
+    dp = W.make_dpooled(cfg)
+    lr = 0.03
+    tables, grad, view, status = _run_bwd(cfg, host, offsets, indices, dp, lr, grad_cap=indices.size)
+    assert status == 0
+    co = oracle.coalesce(cfg["rows"], offsets, indices, B)
+    _check_coalesce(view, co, indices.size)
+    g_ref, g_mag, w_ref, w_mag = oracle.sgd(host, dtype, offsets, B, indices.size, dp, lr, co)
+    U = co["U"]
+    rel = REL[dtype]
+    assert_close(grad.cpu().numpy()[:U], g_ref, g_mag, rel, f"gradient {dtype} d={d}")
+    for t in range(3):
+        us = np.nonzero(co["uniq_table"] == t)[0]
+        rows_t = co["uniq_row"][us]
+        dev = device_table_f64(tables[t], dtype)
+        assert_close(dev[rows_t], w_ref[us], w_mag[us], rel, f"rows {dtype} d={d} t={t}", table_dtype=dtype)
+        untouched = np.ones(cfg["rows"][t], dtype=bool)
+        untouched[rows_t] = False
+        np.testing.assert_array_equal(device_table_bits(tables[t])[untouched],
+                                      host_table_bits(host[t], dtype)[untouched])
+
+
 def test_all_duplicate_bag_gives_k_times_the_gradient():
     k = 1300
     host = [np.zeros((9, 16), np.float32)]

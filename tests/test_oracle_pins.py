@@ -599,3 +599,33 @@ def test_int4_pooling_sums_the_decoded_rows():
         for bb in range(B):
             lo, hi = offsets[t * B + bb], offsets[t * B + bb + 1]
             np.testing.assert_allclose(pooled[bb, t], dec[indices[lo:hi]].sum(axis=0), rtol=1e-14, atol=1e-14)
+
+
+# ------------------------------------------------------ the parallel build ---
+
+def test_openmp_build_gives_identical_results():
+    # the OpenMP build of the oracle (used only to time it on all host cores)
+    # computes every output element in the same order: identical bits
+    cfg = W.make_config("multi-hot", B=200, rows=[5000, 70000, 123, 9])
+    host = W.tables_host(cfg)
+    off, idx = W.make_indices(cfg)
+    e0, dy = W.make_e0(cfg), W.make_dy(cfg)
+
+    def run():
+        p, pm = oracle.emb_bag_fwd(host, "f16", off, idx, cfg["B"])
+        y = oracle.interact_fwd(e0, p, False, emb_mag=pm)
+        a = oracle.interact_bwd(e0, p, dy, False, emb_mag=pm)
+        co = oracle.coalesce(cfg["rows"], off, idx, cfg["B"])
+        s = oracle.sgd(host, "f16", off, cfg["B"], idx.size, a[2], 0.01, co, dpooled_mag=a[3])
+        g = oracle.adagrad(host, "f16", off, cfg["B"], idx.size, a[2], 0.01, 1e-8, np.ones(co["U"]), co)
+        return [p, pm, *y, *a, *s, *g]
+
+    try:
+        serial = run()
+        if not oracle.use_openmp(True):
+            pytest.skip("no OpenMP build of the oracle on this host")
+        parallel = run()
+    finally:
+        oracle.use_openmp(False)
+    for x, z in zip(serial, parallel):
+        np.testing.assert_array_equal(x, z)
