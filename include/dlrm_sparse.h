@@ -427,6 +427,31 @@ int dlrm_emb_bag_bwd_sgd_noalloc(void *const *tables, const int64_t *rows, int T
                                  int64_t grad_rows_cap, dlrm_coalesced_view *view,
                                  int32_t *err_flag, dlrm_stream_t stream);
 
+/*
+ * Testing aid (the pages have no counterpart): makes the kernels' bounded
+ * waits run out on purpose, so that a test can check what a wait that gives
+ * up does.  A process-wide setting, read when a call launches its kernels;
+ * calls already enqueued are not affected.  Results of calls made while a
+ * hook is set are invalid; set all three back to their defaults (-1, 0, -1)
+ * afterwards.
+ *  sort_wait_polls   polls of one look-back word by the radix sort's passes
+ *                    before the wait gives up (negative: the default, about
+ *                    a second; at most the default).
+ *  sort_first_tile   the first tile the passes claim (0: normal).  k > 0
+ *                    leaves tiles 0 .. k-1 unclaimed, so the pass's tile k
+ *                    waits for counts that never come and gives up:
+ *                    DLRM_FLAG_WAIT_TIMEOUT is raised, every write stays in
+ *                    the workspace, and the reduce that follows updates no
+ *                    table row (it checks the coalescing's failure word).
+ *  copy_wait_polls   polls of a stage barrier in the main loop of the
+ *                    bulk-copy (CUDA-core) interaction forward (negative: the
+ *                    default; 0: give up at once).  A CTA that gives up waits,
+ *                    with the default limit, for its copies in flight, writes
+ *                    NaN into its samples' pair outputs and returns.
+ * Returns DLRM_OK, or DLRM_ERR_INVALID_ARG for a negative sort_first_tile.
+ */
+int dlrm_set_wait_test_hooks(int64_t sort_wait_polls, int sort_first_tile, int64_t copy_wait_polls);
+
 /* Synchronizes the stream, reads the flag and maps its bits to a status
  * (DLRM_OK if no bit is set).  A CUDA failure returns DLRM_ERR_CUDA. */
 int dlrm_read_error(const int32_t *err_flag, dlrm_stream_t stream);

@@ -44,6 +44,7 @@ SIGNATURES = {
                                  _i64, _vp, _i64, _vp]),
     "dlrm_set_interact_kernel": (_i32, [_i32]),
     "dlrm_get_interact_kernel": (_i32, []),
+    "dlrm_set_wait_test_hooks": (_i32, [_i64, _i32, _i64]),
     "dlrm_emb_bag_bwd_workspace_size": (_sz, [_i32, _i64, _i64, _i32]),
     "dlrm_emb_bag_bwd_sgd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64,
                                     _i64, _f32, _vp, _i64, _vp, _sz, ctypes.POINTER(CoalescedView),
@@ -179,6 +180,14 @@ def dlrm_set_interact_kernel(kind: int) -> None:
     """Kernel family of the interaction calls: INTERACT_KERNEL_AUTO (tensor cores
     where they apply) or INTERACT_KERNEL_CUDA_CORE (process-wide)."""
     _check(load().dlrm_set_interact_kernel(int(kind)), "dlrm_set_interact_kernel")
+
+
+def dlrm_set_wait_test_hooks(sort_wait_polls: int = -1, sort_first_tile: int = 0,
+                             copy_wait_polls: int = -1) -> None:
+    """Testing aid: shortens the kernels' bounded waits (see the C header);
+    the defaults restore normal operation."""
+    _check(load().dlrm_set_wait_test_hooks(sort_wait_polls, sort_first_tile, copy_wait_polls),
+           "dlrm_set_wait_test_hooks")
 
 
 def dlrm_get_interact_kernel() -> int:

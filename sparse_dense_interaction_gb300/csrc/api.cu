@@ -49,6 +49,21 @@ int sm_count()
 
 static std::atomic<int> g_interact_kernel{DLRM_INTERACT_KERNEL_AUTO};
 
+// testing hook of the bounded waits (negative: the kernel's default)
+static std::atomic<int64_t> g_hook_sort_polls{-1}, g_hook_copy_polls{-1};
+static std::atomic<uint32_t> g_hook_first_tile{0};
+
+WaitHooks wait_hooks(int default_sort_polls, int default_copy_polls)
+{
+    WaitHooks h;
+    const int64_t sp = g_hook_sort_polls.load(std::memory_order_relaxed);
+    const int64_t cp = g_hook_copy_polls.load(std::memory_order_relaxed);
+    h.sort_polls = sp < 0 ? default_sort_polls : (int)(sp < default_sort_polls ? sp : default_sort_polls);
+    h.copy_polls = cp < 0 ? default_copy_polls : (int)(cp < default_copy_polls ? cp : default_copy_polls);
+    h.sort_first_tile = g_hook_first_tile.load(std::memory_order_relaxed);
+    return h;
+}
+
 bool interact_tensor_cores() { return g_interact_kernel.load(std::memory_order_relaxed) == DLRM_INTERACT_KERNEL_AUTO; }
 
 // kernels (defined in the other translation units)
@@ -219,6 +234,16 @@ int dlrm_set_interact_kernel(int kind)
 }
 
 int dlrm_get_interact_kernel(void) { return dlrm::g_interact_kernel.load(std::memory_order_relaxed); }
+
+int dlrm_set_wait_test_hooks(int64_t sort_wait_polls, int sort_first_tile, int64_t copy_wait_polls)
+{
+    if (sort_first_tile < 0)
+        return DLRM_ERR_INVALID_ARG;
+    dlrm::g_hook_sort_polls.store(sort_wait_polls < 0 ? -1 : sort_wait_polls, std::memory_order_relaxed);
+    dlrm::g_hook_copy_polls.store(copy_wait_polls < 0 ? -1 : copy_wait_polls, std::memory_order_relaxed);
+    dlrm::g_hook_first_tile.store((uint32_t)sort_first_tile, std::memory_order_relaxed);
+    return DLRM_OK;
+}
 
 int dlrm_interact_fwd(const float *e0, int64_t e0_stride, const float *emb, int64_t emb_sample_stride,
                       int N, int d, int64_t B, int mode, float *y, int64_t y_stride,

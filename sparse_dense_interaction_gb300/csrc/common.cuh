@@ -33,6 +33,16 @@ int allow_dynamic_smem(const void *kernel, int bytes, std::atomic<unsigned long 
 // Whether the interaction calls may take the tensor-core kernels (the
 // process-wide setting of dlrm_set_interact_kernel).
 bool interact_tensor_cores();
+// Limits of the kernels' bounded waits for the next launches, as the testing
+// hook dlrm_set_wait_test_hooks left them (defaults when unset): polls of a
+// radix pass's look-back word, the first tile the passes claim, polls of a
+// stage barrier in the main loop of the bulk-copy interaction forward.
+struct WaitHooks {
+    int sort_polls;
+    uint32_t sort_first_tile;
+    int copy_polls;
+};
+WaitHooks wait_hooks(int default_sort_polls, int default_copy_polls);
 // Host checks shared by the entry points (api.cu): the table arguments (fills
 // the kernel-parameter view), and the whole argument list of the backward with
 // SGD (the call without a workspace passes its fixed scratch as workspace).

@@ -58,7 +58,7 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.seg_off = take(n4 + 4);
     L.status[0] = take((size_t)kRadix * L.ntiles_max * 8);
     L.status[1] = take((size_t)kRadix * L.ntiles_max * 8);
-    L.tile_ctr = take((size_t)kMaxPasses * 4);
+    L.tile_ctr = take(((size_t)kMaxPasses + 1) * 4);  // the passes' tile counters, then the sort-failed word
     L.tile_hist = take((size_t)L.ntiles_max * 2 * kMaxPasses * kRadix * 4);
     L.counts = take((size_t)kMaxPasses * T * kRadix * 4);
     L.tstart = take(((size_t)T + 1) * 4);
@@ -81,7 +81,7 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
 
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nnz, BwdPtrs w,
-                int32_t *err)
+                uint32_t first_tile, int32_t *err)
 {
     __shared__ int64_t start[DLRM_MAX_TABLES + 1];
     for (int t = threadIdx.x; t <= T; t += blockDim.x)
@@ -114,7 +114,9 @@ bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t n
     for (int t = threadIdx.x; t <= T; t += blockDim.x)
         w.tstart[t] = (uint32_t)start[t];
     if (threadIdx.x < kMaxPasses)
-        w.tile_ctr[threadIdx.x] = 0;
+        w.tile_ctr[threadIdx.x] = first_tile;  // 0 unless a test leaves the first tiles unclaimed
+    if (threadIdx.x == kMaxPasses)
+        *w.sort_failed = 0;
 }
 
 // ------------------------------------------------------------- bag ids ---
@@ -288,7 +290,7 @@ sort_digit_scan_kernel(int passes, int T, BwdPtrs w)
 // count and needs no other ordering.
 constexpr uint32_t kAggregate = 1u;  // the tile's own count of the digit
 constexpr uint32_t kInclusive = 2u;  // count of the digit in this and all earlier tiles of the table
-constexpr int kSpinLimit = 1 << 20;  // polls of one word before a wait gives up (about a second)
+constexpr int kSpinLimit = 1 << 20;  // default polls of one word before a wait gives up (about a second)
 
 __device__ __forceinline__ void store_status(uint64_t *p, uint32_t kind, uint32_t count)
 {
@@ -311,7 +313,7 @@ __device__ __forceinline__ uint64_t load_status(const uint64_t *p)
 // DLRM_FLAG_WAIT_TIMEOUT and writes stay inside the table's range.
 __global__ void __launch_bounds__(kSortThreads, 4)
 sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__ indices, TableSet ts, int T,
-                     BwdPtrs w, int32_t *err)
+                     BwdPtrs w, int spin_limit, int32_t *err)
 {
     __shared__ uint32_t skey[kTile];
     __shared__ uint32_t sval[kTile];
@@ -425,7 +427,7 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
                 const uint64_t v = load_status(stat + (size_t)k * kRadix + tid);
                 const uint32_t kind = (uint32_t)(v >> 32);
                 if (kind == 0u) {
-                    if (++spins > kSpinLimit) {
+                    if (++spins > spin_limit) {
                         timed_out = 1;
                         break;
                     }
@@ -441,8 +443,10 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
         gbase[tid] = w.counts[((size_t)pass * T + ti.t) * kRadix + tid] + excl;
     }
     __syncthreads();
-    if (tid == 0 && timed_out)
+    if (tid == 0 && timed_out) {
         raise_flag(err, DLRM_FLAG_WAIT_TIMEOUT);
+        atomicOr(w.sort_failed, 1u);
+    }
     const uint32_t n = ti.hi - ti.lo;
     const uint32_t tbeg = w.tstart[ti.t], tlen = w.tstart[ti.t + 1] - tbeg;
     for (uint32_t j = tid; j < n; j += kSortThreads) {
@@ -597,6 +601,7 @@ static BwdPtrs bind_workspace(int T, int64_t nnz, int d, void *workspace)
     w.status[0] = reinterpret_cast<uint64_t *>(base + L.status[0]);
     w.status[1] = reinterpret_cast<uint64_t *>(base + L.status[1]);
     w.tile_ctr = reinterpret_cast<uint32_t *>(base + L.tile_ctr);
+    w.sort_failed = w.tile_ctr + kMaxPasses;
     w.tile_hist = reinterpret_cast<uint32_t *>(base + L.tile_hist);
     w.counts = reinterpret_cast<uint32_t *>(base + L.counts);
     w.tstart = reinterpret_cast<uint32_t *>(base + L.tstart);
@@ -641,8 +646,9 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
         view->num_unique = w.num_unique;
     }
 
+    const WaitHooks hooks = wait_hooks(kSpinLimit, 0);
     int s;
-    bwd_prep_kernel<<<1, 256, 0, st>>>(offsets, T, B, nnz, w, err);
+    bwd_prep_kernel<<<1, 256, 0, st>>>(offsets, T, B, nnz, w, hooks.sort_first_tile, err);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
@@ -671,7 +677,8 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
     int shift = 0;
     for (int p = 0; p < passes; p++) {
         const int nb = pass_bits(bits, passes, p);
-        sort_onesweep_kernel<<<(unsigned)grid, kSortThreads, 0, st>>>(p, shift, nb, indices, ts, T, w, err);
+        sort_onesweep_kernel<<<(unsigned)grid, kSortThreads, 0, st>>>(p, shift, nb, indices, ts, T, w,
+                                                                      hooks.sort_polls, err);
         count_launch(st);
         if ((s = launch_status()) != DLRM_OK)
             return s;

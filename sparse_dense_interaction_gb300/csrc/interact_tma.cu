@@ -52,11 +52,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
 }
 
 // true once the phase of the given parity has completed; gives up after
-// kSpinLimitTma polls
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// `polls` polls
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int polls = kSpinLimitTma)
 {
     uint32_t done = 0;
-    for (int it = 0; it < kSpinLimitTma && !done; it++)
+    for (int it = 0; it < polls && !done; it++)
         asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
                      : "=r"(done)
                      : "r"(smem_u32(bar)), "r"(parity)
@@ -87,7 +87,8 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 template <int KS>  // lanes per tile
 __global__ void __launch_bounds__(512, 2)
 interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid_constant__ CUtensorMap map_e0,
-                        int N, int d, int64_t B, int mode, float *__restrict__ y, int64_t ys, int S, int R8)
+                        int N, int d, int64_t B, int mode, float *__restrict__ y, int64_t ys, int S, int R8,
+                        int wait_polls)
 {
     extern __shared__ unsigned char smem_raw[];
     const int inc = mode & kInteractSelf;
@@ -172,7 +173,7 @@ interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __gri
     int waited = 0;  // chunks whose stage this CTA has seen complete
     for (int c = 0; c < nchunks; c++) {
         const int st = c & 1;
-        if (!mbar_wait(&bar[st], (uint32_t)((c >> 1) & 1)))
+        if (!mbar_wait(&bar[st], (uint32_t)((c >> 1) & 1), wait_polls))
             failed = 1;
         __syncthreads();
         if (failed)
@@ -241,9 +242,10 @@ interact_fwd_tma_kernel(const __grid_constant__ CUtensorMap map_emb, const __gri
 
     if (failed) {
         // copies still in flight target this CTA's shared memory: wait for
-        // them (bounded) before leaving, and poison the outputs
+        // them (bounded by the default limit, whatever the main loop's) before
+        // leaving, and poison the outputs
         for (int c = waited; c < nchunks && c < waited + 2; c++)
-            mbar_wait(&bar[c & 1], (uint32_t)((c >> 1) & 1));
+            mbar_wait(&bar[c & 1], (uint32_t)((c >> 1) & 1), kSpinLimitTma);
         __syncthreads();
         for (int64_t li = tid; li < (int64_t)nS * P; li += blockDim.x) {
             const int ss = (int)(li / P);
@@ -346,7 +348,9 @@ int launch_interact_fwd_tma(const float *e0, int64_t e0s, const float *emb, int6
         DLRM_OK)
         return DLRM_ERR_CUDA;
     const int64_t grid = (B + S - 1) / S;
-    interact_fwd_tma_kernel<KS><<<(unsigned)grid, threads, smem, st>>>(map_emb, map_e0, N, d, B, mode, y, ys, S, R8);
+    const int wait_polls = wait_hooks(0, kSpinLimitTma).copy_polls;  // the default unless a test shortens it
+    interact_fwd_tma_kernel<KS><<<(unsigned)grid, threads, smem, st>>>(map_emb, map_e0, N, d, B, mode, y, ys, S, R8,
+                                                                       wait_polls);
     count_launch(st);
     return launch_status();
 }

@@ -113,6 +113,8 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     __shared__ uint32_t cbase[NS];
     __shared__ TileInfo ti;
     __shared__ uint32_t key_before, key_after;
+    if (*w.sort_failed)  // the coalescing gave up a wait: its results are invalid, update nothing
+        return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0)
         find_tile(blockIdx.x, a.T, w.tile_base, w.tstart, ti);
@@ -394,6 +396,8 @@ template <int VEC>
 __global__ void __launch_bounds__(256)
 seg_block_sum_kernel(ReduceArgs a, BwdPtrs w, int NS)
 {
+    if (*w.sort_failed)
+        return;
     using V = Vec<VEC>;
     using F = typename V::F;
     constexpr int EB = 32 * VEC;
@@ -427,6 +431,8 @@ template <typename TT, int VEC, int NB>
 __global__ void __launch_bounds__(256)
 seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
 {
+    if (*w.sort_failed)
+        return;
     using V = Vec<VEC>;
     using F = typename V::F;
     constexpr int EB = 32 * VEC;
