@@ -57,6 +57,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement (kernel experiments)")
     p.add_argument("--schedule", choices=["overlap", "serial"], default="overlap",
                    help="overlap: the backward's coalescing runs on a side stream next to the forward")
     p.add_argument("--optimizer", choices=["sgd", "adagrad"], default="sgd",
@@ -665,7 +666,7 @@ def run_ours(args):
     gathered = st.nnz * cfg["d"] * es / (kernel_ms[fwd_key] / 1e3) / 1e9
 
     # end to end through the public API with host buffers
-    e2e = e2e_measure(args, st, torch, sdi, stream, dev)
+    e2e = None if args.no_e2e else e2e_measure(args, st, torch, sdi, stream, dev)
 
     status = sdi.dlrm_read_error(st.flag)
     if status != 0:
