@@ -673,7 +673,10 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
 // of its own), 4-byte asynchronous copies bring the unit's pair gradients
 // once (a row of dy need not be 16-byte aligned).  The converters write the
 // chunk's A into tensor memory (no shared-memory write) and its columns of Gs
-// into shared memory (published to the tensor core by a proxy fence).
+// into shared memory (published to the tensor core by a proxy fence).  Gs
+// depends on the sample only: a CTA takes the d tiles of each of its samples
+// one after the other and builds the sample's Gs once, into one shared-memory
+// slot per chunk that the MMAs of all its tiles read.
 // Accumulators of Np rounded up to 32 columns fill tensor-memory columns
 // 0 .. 255 (8, 4 or 2 of them), drained by two epilogue groups (warps 0..3
 // and 4..7, alternate units: the writes of dZ, row i as 32 consecutive floats
@@ -689,6 +692,7 @@ constexpr uint32_t kBwcACol = 256;  // A chunk slots at 256 + 64 a (hi at +0, lo
 constexpr int kBwcMaxAS = 4;
 constexpr int kBwcMaxDS = 8;        // pair-gradient slots (units)
 constexpr int kBwcMaxAcc = 8;       // accumulators of W = Np rounded up to 32 columns in columns 0 .. 255
+constexpr int kBwcMaxChunks = 4;    // K chunks of 32 vectors (F <= 128): one Gs slot each
 
 }  // namespace
 
@@ -711,7 +715,6 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
     const int P = (int)num_pairs_of(F, inc);
     const int nd = (d + 127) / 128;  // d tiles
     const int nkc = (F + 31) / 32;   // K chunks of 32 vectors
-    const int64_t nunits = B * nd;
     const int64_t poff = along ? (int64_t)F * d : d;  // first pair column of dy
     const uint32_t rs = (uint32_t)bx * 4u;             // bytes of a raw row
     const uint32_t zslot = (33u * rs + 1023u) & ~1023u;           // 32 chunk rows, then e0
@@ -721,8 +724,8 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
     const uint32_t nacc = 256u / W;                               // accumulators: 8, 4 or 2
 
     unsigned char *zring = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);  // [NR]
-    unsigned char *bring = zring + (size_t)NR * zslot;                                     // [AS] B hi, B lo
-    unsigned char *dring = bring + (size_t)AS * 2 * bbytes;                                // [DS]
+    unsigned char *bring = zring + (size_t)NR * zslot;                                     // [nkc] B hi, B lo
+    unsigned char *dring = bring + (size_t)nkc * 2 * bbytes;                               // [DS]
     uint64_t *zfull = reinterpret_cast<uint64_t *>(dring + (size_t)DS * dslot);             // [NR]
     uint64_t *zempty = zfull + NR;                                                         // [NR]
     uint64_t *dfull = zempty + NR;                                                         // [DS]
@@ -731,6 +734,8 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
     uint64_t *aempty = afull + AS;                                                         // [AS]
     uint64_t *tfull = aempty + AS;                                                         // [nacc]
     uint64_t *tempty = tfull + kBwcMaxAcc;                                                 // [nacc]
+    uint64_t *bfull = tempty + kBwcMaxAcc;                                                 // [nkc]
+    uint64_t *bempty = bfull + kBwcMaxChunks;                                              // [nkc]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -750,6 +755,10 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
             tc::mbar_init(&tfull[b], 1);
             tc::mbar_init(&tempty[b], 128);
         }
+        for (int c = 0; c < nkc; c++) {
+            tc::mbar_init(&bfull[c], 128);
+            tc::mbar_init(&bempty[c], 1);
+        }
         tc::mbar_init(&drain_bar, 1);
         aborted_s = 0;
         tc::mbar_init_fence();
@@ -760,22 +769,28 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_slot;
+    // this CTA's units: its samples b = blockIdx.x + i gridDim.x, the d tiles of each in turn
+    const uint32_t nsamp = blockIdx.x < B ? (uint32_t)((B - 1 - blockIdx.x) / gridDim.x + 1) : 0u;
+    const uint32_t ncta = nsamp * (uint32_t)nd;
+    auto sample_of = [&](uint32_t iu) { return (int64_t)blockIdx.x + (int64_t)(iu / (uint32_t)nd) * gridDim.x; };
 
     if (warp == kBwcTmaWarp) {
         // ---- copies: per unit the pair gradients (all lanes, 4-byte asynchronous copies), per
         // chunk the raw rows of Z (lane 0, bulk tensor copies)
-        uint32_t iu = 0, ic = 0;
+        uint32_t ic = 0;
         bool stop = false;
-        for (int64_t u = blockIdx.x; u < nunits && !stop; u += gridDim.x, iu++) {
-            const int64_t b = u / nd;
-            const int x = (int)(u - b * nd) * 128;
+        for (uint32_t iu = 0; iu < ncta && !stop; iu++) {
+            const int64_t b = sample_of(iu);
+            const int tile = (int)(iu % (uint32_t)nd), x = tile * 128;
             const uint32_t ds = iu % (uint32_t)DS, dph = iu / (uint32_t)DS;
             if (dph > 0 && !tc::mbar_wait(&dempty[ds], (dph - 1) & 1, aborted))
                 break;
-            unsigned char *dd = dring + (size_t)ds * dslot;
-            const float *src = dy + b * dys + poff;
-            for (int p = lane; p < P; p += 32)
-                tc::cp_async4(dd + p * 4, src + p, true);
+            if (tile == 0) {  // the sample's pair gradients (its other tiles reuse its Gs)
+                unsigned char *dd = dring + (size_t)ds * dslot;
+                const float *src = dy + b * dys + poff;
+                for (int p = lane; p < P; p += 32)
+                    tc::cp_async4(dd + p * 4, src + p, true);
+            }
             tc::cp_async_arrive(&dfull[ds]);
             for (int c = 0; c < nkc; c++, ic++) {
                 const uint32_t zs = ic % (uint32_t)NR, zph = ic / (uint32_t)NR;
@@ -804,9 +819,11 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
         // units e = a, a + 128, .. of the chunk's Np x 32 block (row e / 8, columns 4 (e % 8) ..)
         const int a = tid - kBwcConvWarp0 * 32;
         const uint32_t lane_base = (uint32_t)(warp & 3) * 32 << 16;
-        uint32_t iu = 0, ic = 0;
+        uint32_t ic = 0;
         bool stop = false;
-        for (int64_t u = blockIdx.x; u < nunits && !stop; u += gridDim.x, iu++) {
+        for (uint32_t iu = 0; iu < ncta && !stop; iu++) {
+            const int tile = (int)(iu % (uint32_t)nd);
+            const uint32_t sc = iu / (uint32_t)nd;  // the sample's index among this CTA's
             const uint32_t ds = iu % (uint32_t)DS, dph = iu / (uint32_t)DS;
             if (!tc::mbar_wait(&dfull[ds], dph & 1, aborted))
                 break;
@@ -834,10 +851,14 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                     stop = true;
                     break;
                 }
+                if (tile == 0 && sc > 0 && !tc::mbar_wait(&bempty[c], (sc - 1) & 1, aborted)) {
+                    stop = true;
+                    break;
+                }
                 tc::fence_after_sync();
-                unsigned char *bh = bring + (size_t)as * 2 * bbytes;
+                unsigned char *bh = bring + (size_t)c * 2 * bbytes;
                 const int sh = inc ? 1 : -1;  // row i of the pairs starts at i (i + sh) / 2
-                for (int e = a; e < Np * 8; e += 128) {
+                for (int e = a; e < Np * 8 && tile == 0; e += 128) {
                     const int n = e >> 3, q = e & 7;
                     float h[4], l[4];
 #pragma unroll
@@ -862,6 +883,8 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                 tc::fence_async_smem();
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
+                if (tile == 0)
+                    tc::mbar_arrive(&bfull[c]);
                 tc::mbar_arrive(&afull[as]);
                 if (c == nkc - 1)
                     tc::mbar_arrive(&dempty[ds]);  // the unit's pair gradients have been read
@@ -870,9 +893,11 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
     } else if (warp == kBwcMmaWarp) {
         if (lane == 0) {
             const uint32_t idesc = tc::tf32_idesc(128, Np);
-            uint32_t iu = 0, ic = 0;
+            uint32_t ic = 0;
             bool issued = false, ok = true;
-            for (int64_t u = blockIdx.x; u < nunits && ok; u += gridDim.x, iu++) {
+            for (uint32_t iu = 0; iu < ncta && ok; iu++) {
+                const int tile = (int)(iu % (uint32_t)nd);
+                const uint32_t sc = iu / (uint32_t)nd;
                 const uint32_t buf = iu % nacc, v = iu / nacc;
                 if (v > 0 && !tc::mbar_wait(&tempty[buf], (v - 1) & 1, aborted))
                     break;
@@ -880,13 +905,14 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                 const uint32_t dt = tmem + buf * W;
                 for (int c = 0; c < nkc; c++, ic++) {
                     const uint32_t as = ic % (uint32_t)AS, av = ic / (uint32_t)AS;
-                    if (!tc::mbar_wait(&afull[as], av & 1, aborted)) {
+                    if (!tc::mbar_wait(&afull[as], av & 1, aborted) ||
+                        (tile == 0 && !tc::mbar_wait(&bfull[c], sc & 1, aborted))) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
                     const uint32_t ta = tmem + kBwcACol + 64 * as;
-                    const uint32_t bh = tc::smem_u32(bring + (size_t)as * 2 * bbytes), bl = bh + bbytes;
+                    const uint32_t bh = tc::smem_u32(bring + (size_t)c * 2 * bbytes), bl = bh + bbytes;
                     const int ksteps = min(4, (F - 32 * c + 7) / 8);
                     for (int kk = 0; kk < ksteps; kk++) {
                         const uint64_t bhd = tc::sw128_desc(bh + 32u * kk), bld = tc::sw128_desc(bl + 32u * kk);
@@ -897,6 +923,8 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                     }
                     issued = true;
                     tc::mma_commit(&aempty[as]);
+                    if (tile == nd - 1)
+                        tc::mma_commit(&bempty[c]);  // the sample's last tile has read its Gs chunk
                 }
                 if (!ok)
                     break;
@@ -911,20 +939,18 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
         // accumulator = column m of the unit's d tile
         const int g = warp >> 2, et = tid & 127;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        auto load_g0 = [&](int64_t u) -> float {
-            const int64_t b = u / nd;
-            const int m = (int)(u - b * nd) * 128 + et;
-            return (u < nunits && m < d) ? __ldg(dy + b * dys + m) : 0.f;
+        auto load_g0 = [&](uint32_t iu) -> float {
+            const int64_t b = sample_of(iu);
+            const int m = (int)(iu % (uint32_t)nd) * 128 + et;
+            return (iu < ncta && m < d) ? __ldg(dy + b * dys + m) : 0.f;
         };
-        float g0n = load_g0(blockIdx.x + (int64_t)g * gridDim.x);
-        uint32_t iu = g;
-        for (int64_t u = blockIdx.x + (int64_t)g * gridDim.x; u < nunits;
-             u += kBwcEpiGroups * (int64_t)gridDim.x, iu += kBwcEpiGroups) {
-            const int64_t b = u / nd;
-            const int m = (int)(u - b * nd) * 128 + et;
+        float g0n = load_g0((uint32_t)g);
+        for (uint32_t iu = (uint32_t)g; iu < ncta; iu += kBwcEpiGroups) {
+            const int64_t b = sample_of(iu);
+            const int m = (int)(iu % (uint32_t)nd) * 128 + et;
             const bool act = m < d;
             const float g0 = g0n;
-            g0n = load_g0(u + kBwcEpiGroups * (int64_t)gridDim.x);
+            g0n = load_g0(iu + kBwcEpiGroups);
             const uint32_t buf = iu % nacc;
             const bool okw = tc::mbar_wait(&tfull[buf], (iu / nacc) & 1, aborted);
             if (!__all_sync(0xffffffffu, okw))
@@ -965,9 +991,9 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
     }
     if (*aborted) {
         const float nan = __int_as_float(0x7fc00000);
-        for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
-            const int64_t b = u / nd;
-            const int m0 = (int)(u - b * nd) * 128;
+        for (uint32_t iu = 0; iu < ncta; iu++) {
+            const int64_t b = sample_of(iu);
+            const int m0 = (int)(iu % (uint32_t)nd) * 128;
             for (int m = m0 + tid; m < d && m < m0 + 128; m += blockDim.x) {
                 de0[b * de0s + m] = nan;
                 for (int i = 1; i < F; i++)
@@ -1079,14 +1105,13 @@ static int launch_interact_bwd_tc_chunked(const float *e0, int64_t e0s, const fl
     const size_t zslot = (33 * (size_t)bx * 4 + 1023) & ~(size_t)1023;
     const size_t dslot = ((size_t)P * 4 + 127) & ~(size_t)127;
     const size_t bslot = 2 * (size_t)Np * 128;
-    const size_t fixed = 1024 + (size_t)kBwcMaxAcc * 16;
-    // operand slots: up to 4 (tensor memory), pair-gradient slots and raw chunks: as many as fit, up to 8
+    const int nkc = (F + 31) / 32;  // one Gs slot per K chunk, reused by the sample's d tiles
+    const size_t fixed = 1024 + (size_t)kBwcMaxAcc * 16 + (size_t)kBwcMaxChunks * 16 + (size_t)nkc * bslot;
+    // A operand slots: 4 (tensor memory); pair-gradient slots and raw chunks: as many as fit, up to 8
     int AS = kBwcMaxAS, NR = 2, DS = 2;
     auto total = [&](int as, int nr, int ds) {
-        return fixed + (size_t)as * (bslot + 16) + (size_t)nr * (zslot + 16) + (size_t)ds * (dslot + 16);
+        return fixed + (size_t)as * 16 + (size_t)nr * (zslot + 16) + (size_t)ds * (dslot + 16);
     };
-    while (AS > 2 && total(AS, NR, DS) > kMaxSmem)
-        AS--;
     for (bool grew = true; grew;) {
         grew = false;
         if (NR < 8 && total(AS, NR + 1, DS) <= kMaxSmem) {

@@ -141,6 +141,8 @@ INTER_CASES = [  # (B, N, d, include_self)
     # two and three chunks of 32 vectors
     (5000, 13, 64, True), (4900, 31, 256, False), (2500, 20, 200, True), (4900, 40, 64, False),
     (4900, 70, 64, True),
+    # two chunks of vectors over two d tiles, the second ragged (a sample's tiles share its Gs)
+    (2500, 45, 200, True),
 ]
 
 KERNELS = {"auto": sdi.INTERACT_KERNEL_AUTO, "cuda-core": sdi.INTERACT_KERNEL_CUDA_CORE}
