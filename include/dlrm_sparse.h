@@ -225,7 +225,11 @@ int dlrm_get_interact_kernel(void);
  * optional (NULL: not written), with strides in elements.  The pooled values
  * equal dlrm_emb_bag_fwd's bit for bit; y equals dlrm_interact_fwd's within
  * the accuracy of the two (fp32 dot products summed in another order, or the
- * tensor-core split's 2^-20 of |z_i||z_j| per product).
+ * tensor-core split's 2^-20 of |z_i||z_j| per product).  When `pooled` is
+ * given (pooled_table_stride == d) and the tensor-core interaction takes the
+ * operands, the call runs the lookup into `pooled` and then that interaction:
+ * in training the pooled block is written anyway, and the tensor-core
+ * interaction is faster than the single kernel's CUDA-core dot products.
  * T may be 1 .. 127.  The single-kernel path needs rows of a whole number of
  * 16-byte chunks up to 1 KB, 16-byte aligned tables (and pooled, with
  * strides that are multiples of 4), and a Z block of each sample that fits

@@ -1014,13 +1014,19 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
 
 static bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
+// Whether the tensor-core forward takes these operands (d < 32 leaves most of a
+// 32-column chunk empty: the CUDA-core kernels are faster there).
+bool interact_fwd_tc_applies(const float *e0, int64_t e0s, const float *emb, int64_t embs, int N, int d, int64_t B)
+{
+    return interact_tensor_cores() && N >= 1 && N + 1 <= 128 && d >= 32 && d % 4 == 0 && e0s % 4 == 0 &&
+           embs % 4 == 0 && aligned16(e0) && aligned16(emb) && B <= 0x7fffffff;
+}
+
 int launch_interact_fwd_tc(const float *e0, int64_t e0s, const float *emb, int64_t embs, int N, int d, int64_t B,
                            int mode, float *y, int64_t ys, cudaStream_t st)
 {
     const int F = N + 1;
-    // d < 32 leaves most of a 32-column chunk empty: the CUDA-core kernels are faster there
-    if (N < 1 || F > 128 || d < 32 || d % 4 != 0 || e0s % 4 != 0 || embs % 4 != 0 || !aligned16(e0) ||
-        !aligned16(emb) || B > 0x7fffffff)
+    if (!interact_fwd_tc_applies(e0, e0s, emb, embs, N, d, B))
         return 1;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc)
