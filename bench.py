@@ -565,6 +565,13 @@ def measure_target(name, args, dev, update="sorted"):
             gbs = nbytes / (ms / 1e3) / 1e9
             e.update(bytes=nbytes, gbs=gbs, frac=gbs / peak)
         stages[stage] = e
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):  # DRAM bytes of a full launch from ncu (scaled from small cases)
+        with open(tpath) as f:
+            tr = json.load(f).get(name, {})
+        for stage, kern in (("reduce", "seg_reduce"), ("backward", "emb_bag_bwd_atomic")):
+            if stage in stages and kern in tr and (stage == "reduce" or update == "atomic"):
+                stages[stage]["traffic"] = tr[kern]
     out = {"config": config_of(cfg), "update": update, "ms_per_step": ms_step,
            "samples_per_s": cfg["B"] / (ms_step / 1e3), "steps": K, "unique_rows": uniq, "lookups": st.nnz,
            "stages": stages}
