@@ -273,8 +273,14 @@ size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d);
  *
  *   g_u = sum over the lookups k of r in table t, in sorted order, of
  *         dpooled[b(k)*dp_sample_stride + t*dp_table_stride + 0 .. d)
- *   tables[t][r] <- tables[t][r] - lr * g_u     (fp32; one rounding to the
- *                                                table type, nearest even)
+ *   tables[t][r] <- tables[t][r] - lr * g_u
+ *
+ * Rounding of the update: fp32 and fp16 tables receive the step -lr * g_u
+ * (computed in fp32, rounded to the table type, nearest even) as one
+ * reduction performed in L2, which rounds the sum once more; bf16 tables are
+ * read, updated in fp32 (one fused multiply-add) and written back with one
+ * rounding.  Every unique row is updated exactly once per call, so results
+ * are reproducible bit for bit from run to run.
  *
  * Rows no lookup touches are not written.  lr == 0 leaves the tables
  * untouched (the coalesced gradient only).

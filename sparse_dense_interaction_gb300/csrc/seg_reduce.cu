@@ -81,6 +81,57 @@ struct RowChunk {
     }
 };
 
+// The SGD update of fp32 and fp16 rows as one reduction performed in L2: the
+// step -lr*g is computed in fp32, rounded to the table type and added to the
+// row (rounded again); nothing waits for the row.  Each unique row receives
+// one such update per launch (its run's whole sum), so the result does not
+// depend on timing.  bf16 rows keep the read-modify-write (one rounding):
+// their 8-bit significand leaves too little room for two.
+template <typename TT, int VEC>
+struct RedUpdate {
+    static constexpr bool kUse = false;
+    __device__ __forceinline__ static void apply(TT *, const typename Vec<VEC>::F &, float) {}
+};
+template <>
+struct RedUpdate<float, 4> {
+    static constexpr bool kUse = true;
+    __device__ __forceinline__ static void apply(float *p, const float4 &g, float lr)
+    {
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(-lr * g.x), "f"(-lr * g.y),
+                     "f"(-lr * g.z), "f"(-lr * g.w)
+                     : "memory");
+    }
+};
+template <>
+struct RedUpdate<float, 1> {
+    static constexpr bool kUse = true;
+    __device__ __forceinline__ static void apply(float *p, float g, float lr)
+    {
+        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(-lr * g) : "memory");
+    }
+};
+template <>
+struct RedUpdate<__half, 4> {
+    static constexpr bool kUse = true;
+    __device__ __forceinline__ static void apply(__half *p, const float4 &g, float lr)
+    {
+        const __half2 a = __floats2half2_rn(-lr * g.x, -lr * g.y), b = __floats2half2_rn(-lr * g.z, -lr * g.w);
+        asm volatile("red.global.add.noftz.v2.f16x2 [%0], {%1, %2};" ::"l"(p),
+                     "r"(*reinterpret_cast<const uint32_t *>(&a)), "r"(*reinterpret_cast<const uint32_t *>(&b))
+                     : "memory");
+    }
+};
+template <>
+struct RedUpdate<__half, 1> {
+    static constexpr bool kUse = true;
+    __device__ __forceinline__ static void apply(__half *p, float g, float lr)
+    {
+        const __half h = __float2half_rn(-lr * g);
+        asm volatile("red.global.add.noftz.f16 [%0], %1;" ::"l"(p), "h"(*reinterpret_cast<const unsigned short *>(&h))
+                     : "memory");
+    }
+};
+
 // Asks L2 to fetch the line holding p (no register result, never faults the
 // caller: only called on rows inside the table).
 __device__ __forceinline__ void prefetch_l2(const void *p)
@@ -280,7 +331,10 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                         for (int c = 0; c < C; c++)
                             if (on[c]) {
                                 TT *wp = wtab + (int64_t)cur_row * a.d + eb + (c * G + gl) * VEC;
-                                RC::store(wp, RC::sgd(RC::load(wp), acc[c], step));
+                                if (RedUpdate<TT, VEC>::kUse && !adagrad)
+                                    RedUpdate<TT, VEC>::apply(wp, acc[c], step);
+                                else
+                                    RC::store(wp, RC::sgd(RC::load(wp), acc[c], step));
                             }
                     }
                 }
@@ -292,7 +346,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
 
         const uint32_t c1e = c1 + (U - c1 % U) % U;  // padded end of the walk
         for (uint32_t p0 = c0; p0 < c1e; p0 += U) {
-            if (PD > 0 && update) {
+            if (PD > 0 && update && (adagrad || !RedUpdate<TT, VEC>::kUse)) {
 #pragma unroll
                 for (int u = 0; u < U; u++) {
                     const uint32_t q = p0 + PD * U + u;
@@ -527,7 +581,10 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
                 }
                 if (a.lr != 0.f && (int64_t)row < a.tables.rows[t]) {
                     TT *wp = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t])) + (int64_t)row * a.d + e;
-                    RowChunk<TT, VEC>::store(wp, RowChunk<TT, VEC>::sgd(RowChunk<TT, VEC>::load(wp), acc, a.lr));
+                    if (RedUpdate<TT, VEC>::kUse)
+                        RedUpdate<TT, VEC>::apply(wp, acc, a.lr);
+                    else
+                        RowChunk<TT, VEC>::store(wp, RowChunk<TT, VEC>::sgd(RowChunk<TT, VEC>::load(wp), acc, a.lr));
                 }
             }
         }
