@@ -629,11 +629,14 @@ static int reduce_typed(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, boo
     // 16-lane streams (more chunks per tile, shorter serial walks): two
     // 16-byte pieces per lane for rows of 128+ values, one for rows of up to
     // 64; rows in between keep one 32-lane stream per chunk (a single walk)
+    // (the rows of fp32 and fp16 tables are updated by L2 reductions and never
+    // read here: nothing to prefetch)
+    constexpr int PD = RedUpdate<TT, 4>::kUse ? 0 : 1;
     if (a.d >= 128)
-        return run_reduce<TT, 4, 16, 2, 2, 1>(a, w, grid, st);
+        return run_reduce<TT, 4, 16, 2, 2, PD>(a, w, grid, st);
     if (a.d <= 64)
-        return run_reduce<TT, 4, 16, 1, 2, 1>(a, w, grid, st);
-    return run_reduce<TT, 4, 32, 1, 4, 1>(a, w, grid, st);
+        return run_reduce<TT, 4, 16, 1, 2, PD>(a, w, grid, st);
+    return run_reduce<TT, 4, 32, 1, 4, PD>(a, w, grid, st);
 }
 
 int launch_seg_reduce(int dtype, const ReduceArgs &a, const BwdPtrs &w, int64_t grid, bool vec, cudaStream_t st)
