@@ -59,8 +59,11 @@ __device__ __forceinline__ bool all_of(bool pred, int id, int threads)
 // byte offset of 16-byte unit q of row r in a 128-byte-swizzled tile
 __device__ __forceinline__ uint32_t sw128(int r, int q) { return (uint32_t)r * 128u + ((uint32_t)(q ^ (r & 7)) << 4); }
 
-// Waits for the tensor core to finish what this thread issued, before its
-// tensor memory is freed (bounded; used when the CTA gives up).
+// Waits for the tensor core to finish what this thread issued, and for the
+// barrier arrivals of its earlier commits, before the CTA frees its tensor
+// memory and leaves: no commit may arrive on the shared memory of a CTA that
+// has exited, whether it left normally (nobody waits on the last phases of
+// the slot-free barriers) or gave up.  Bounded.
 __device__ __forceinline__ void drain_mmas(uint64_t *bar)
 {
     tc::mma_commit(bar);
@@ -322,7 +325,7 @@ interact_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
                     break;
                 tc::mma_commit(&tfull[buf]);
             }
-            if (*aborted && issued)
+            if (issued)
                 drain_mmas(&drain_bar);
         }
         __syncwarp();
@@ -584,7 +587,7 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
                 tc::mma_commit(&aempty[as]);
                 tc::mma_commit(&tfull[buf]);
             }
-            if (*aborted && issued)
+            if (issued)
                 drain_mmas(&drain_bar);
         }
         __syncwarp();
@@ -681,18 +684,26 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
 // 0 .. 255 (8, 4 or 2 of them), drained by two epilogue groups (warps 0..3
 // and 4..7, alternate units: the writes of dZ, row i as 32 consecutive floats
 // per warp, are the slow part); each loads the e0 part of dy of its next unit
-// ahead.  One converter group (warps 8..11).  (For F <= 32 the one-chunk
-// kernel above is faster: measured 0.50 vs 0.83 ms on the multi-hot shape.)
+// ahead.  Two converter groups (warps 8..11 and 12..15) take the chunks in
+// turn; with an odd number of raw slots a slot's fills alternate between them,
+// so a group waits for the slot's previous fill to be released before it waits
+// for its own (a parity wait cannot tell a fill from the one two phases on).
+// The tensor pipe bounds the kernel: 3 x ceil(F / 8) MMAs per unit of about
+// 160 to 200 cycles each (M = 128, N = 112, K = 8, A in tensor memory).
+// (For F <= 32 the one-chunk kernel above is faster: measured 0.50 vs 0.83 ms
+// on the multi-hot shape.)
 
 namespace {
 
-constexpr int kBwcEpiGroups = 2, kBwcConvWarp0 = 8, kBwcTmaWarp = 12, kBwcMmaWarp = 13;
-constexpr int kBwcThreads = 448;
+constexpr int kBwcEpiGroups = 2, kBwcConvGroups = 2, kBwcConvWarp0 = 8, kBwcTmaWarp = 16, kBwcMmaWarp = 17;
+constexpr int kBwcThreads = 576;
 constexpr uint32_t kBwcACol = 256;  // A chunk slots at 256 + 64 a (hi at +0, lo at +32); accumulators below
 constexpr int kBwcMaxAS = 4;
 constexpr int kBwcMaxDS = 8;        // pair-gradient slots (units)
 constexpr int kBwcMaxAcc = 8;       // accumulators of W = Np rounded up to 32 columns in columns 0 .. 255
 constexpr int kBwcMaxChunks = 4;    // K chunks of 32 vectors (F <= 128): one Gs slot each
+// each A slot belongs to one converter group (slot ic % AS, group ic % 2), which takes its uses in order
+static_assert(kBwcMaxAS % kBwcConvGroups == 0, "A slots must not alternate between converter groups");
 
 }  // namespace
 
@@ -745,7 +756,7 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
         }
         for (int s = 0; s < DS; s++) {
             tc::mbar_init(&dfull[s], 32);  // one copy arrival per lane of the copy warp
-            tc::mbar_init(&dempty[s], 128);
+            tc::mbar_init(&dempty[s], 128 * kBwcConvGroups);
         }
         for (int s = 0; s < AS; s++) {
             tc::mbar_init(&afull[s], 128);
@@ -763,6 +774,11 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
         aborted_s = 0;
         tc::mbar_init_fence();
     }
+    // the Gs slots start zero: their padding (rows and columns from F on, and the
+    // diagonal for strict pairs) is never written again
+    for (uint32_t o = (uint32_t)tid * 16u; o < (uint32_t)nkc * 2u * bbytes; o += kBwcThreads * 16u)
+        *reinterpret_cast<float4 *>(bring + o) = make_float4(0.f, 0.f, 0.f, 0.f);
+    tc::fence_async_smem();
     if (warp == kBwcMmaWarp)
         tc::tmem_alloc<kTmemCols>(&tmem_slot);
     tc::fence_before_sync();
@@ -815,9 +831,9 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                 }
         __syncwarp();
     } else if (warp >= kBwcConvWarp0 && warp < kBwcTmaWarp) {
-        // ---- converters: thread a writes A lane a; the Gs entries of a chunk are the 16-byte
-        // units e = a, a + 128, .. of the chunk's Np x 32 block (row e / 8, columns 4 (e % 8) ..)
-        const int a = tid - kBwcConvWarp0 * 32;
+        // ---- converters, two groups taking the chunks in turn (group cg the chunks ic with
+        // ic % 2 == cg, counted over all units): thread a writes A lane a
+        const int a = (tid - kBwcConvWarp0 * 32) & 127, cg = (warp - kBwcConvWarp0) >> 2;
         const uint32_t lane_base = (uint32_t)(warp & 3) * 32 << 16;
         uint32_t ic = 0;
         bool stop = false;
@@ -828,10 +844,18 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
             if (!tc::mbar_wait(&dfull[ds], dph & 1, aborted))
                 break;
             const float *dyp = reinterpret_cast<const float *>(dring + (size_t)ds * dslot);
+            // the last of the unit's chunks that this group takes (each takes one at least: nkc >= 2)
+            const int clast = nkc - 1 - (int)(((ic + (uint32_t)nkc - 1u) & 1u) != (uint32_t)cg);
             for (int c = 0; c < nkc; c++, ic++) {
+                if ((ic & 1u) != (uint32_t)cg)
+                    continue;
                 const uint32_t zs = ic % (uint32_t)NR, zph = ic / (uint32_t)NR;
                 const uint32_t as = ic % (uint32_t)AS, av = ic / (uint32_t)AS;
-                if (!tc::mbar_wait(&zfull[zs], zph & 1, aborted)) {
+                // With an odd number of raw slots, consecutive fills of a slot go to alternate groups: a
+                // group must see the slot's previous fill released before it waits for this one, or the
+                // parity wait below would take the phase of the fill before (still in flight) for it.
+                if ((zph > 0 && !tc::mbar_wait(&zempty[zs], (zph - 1) & 1, aborted)) ||
+                    !tc::mbar_wait(&zfull[zs], zph & 1, aborted)) {
                     stop = true;
                     break;
                 }
@@ -857,37 +881,58 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                 }
                 tc::fence_after_sync();
                 unsigned char *bh = bring + (size_t)c * 2 * bbytes;
-                const int sh = inc ? 1 : -1;  // row i of the pairs starts at i (i + sh) / 2
-                for (int e = a; e < Np * 8 && tile == 0; e += 128) {
-                    const int n = e >> 3, q = e & 7;
+                // Gs of rows n < F and the chunk's columns k < F, 4 columns (one 16-byte unit) per
+                // item; the rest of the slot stays zero.  Pair (i, j), j <= i, sits at T(i) + j with
+                // T(i) = i (i + sh) / 2, so T(i + 1) = T(i) + i + inc.
+                const int sh = inc ? 1 : -1;
+                const int kc = min(32, F - 32 * c);
+                const int lq = kc > 16 ? 3 : (kc > 8 ? 2 : (kc > 4 ? 1 : 0));  // items per row: 1 << lq
+                for (int e = a; e < (F << lq) && tile == 0; e += 128) {
+                    const int n = e >> lq, k0 = 32 * c + 4 * (e & ((1 << lq) - 1));
+                    float v[4];
+                    if (n >= k0 + 4) {  // below the diagonal: four consecutive pairs of row n
+                        const float *s = dyp + ((n * (n + sh)) >> 1) + k0;
+#pragma unroll
+                        for (int j = 0; j < 4; j++)
+                            v[j] = s[j];
+                    } else if (n < k0) {  // above it: entry n of rows k0 .. k0 + 3
+                        int t = (k0 * (k0 + sh)) >> 1;
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            v[j] = k0 + j < F ? dyp[t + n] : 0.f;
+                            t += k0 + j + inc;
+                        }
+                    } else {  // the 4 x 4 block on the diagonal
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            const int k = k0 + j, hi = n > k ? n : k, lo = n > k ? k : n;
+                            v[j] = (k < F && (n != k || inc)) ? dyp[((hi * (hi + sh)) >> 1) + lo] : 0.f;
+                            if (n == k)
+                                v[j] *= 2.f;  // a self pair counts in G and in G^T
+                        }
+                    }
                     float h[4], l[4];
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
-                        const int k = 32 * c + 4 * q + j;
-                        float v = 0.f;
-                        if (n < F && k < F && (n != k || inc)) {
-                            const int hi = n > k ? n : k, lo = n > k ? k : n;
-                            v = dyp[((hi * (hi + sh)) >> 1) + lo];
-                            if (n == k)
-                                v *= 2.f;  // a self pair counts in G and in G^T
-                        }
-                        h[j] = tc::tf32_round(v);
-                        l[j] = tc::tf32_round(v - h[j]);
+                        h[j] = tc::tf32_round(v[j]);
+                        l[j] = tc::tf32_round(v[j] - h[j]);
                     }
-                    *reinterpret_cast<float4 *>(bh + sw128(n, q)) = make_float4(h[0], h[1], h[2], h[3]);
-                    *reinterpret_cast<float4 *>(bh + bbytes + sw128(n, q)) = make_float4(l[0], l[1], l[2], l[3]);
+                    const uint32_t o = sw128(n, (k0 & 31) >> 2);
+                    *reinterpret_cast<float4 *>(bh + o) = make_float4(h[0], h[1], h[2], h[3]);
+                    *reinterpret_cast<float4 *>(bh + bbytes + o) = make_float4(l[0], l[1], l[2], l[3]);
                 }
                 const uint32_t ta = tmem + lane_base + kBwcACol + 64 * as;
                 tc::tmem_st32(ta, zh);
                 tc::tmem_st32(ta + 32, zl);
-                tc::fence_async_smem();
+                if (tile == 0)
+                    tc::fence_async_smem();  // the Gs stores, for the tensor core (A is in tensor memory)
                 tc::tmem_st_wait();
                 tc::fence_before_sync();
                 if (tile == 0)
                     tc::mbar_arrive(&bfull[c]);
                 tc::mbar_arrive(&afull[as]);
-                if (c == nkc - 1)
-                    tc::mbar_arrive(&dempty[ds]);  // the unit's pair gradients have been read
+                if (c == clast)
+                    tc::mbar_arrive(&dempty[ds]);  // this group has read the unit's pair gradients
             }
         }
     } else if (warp == kBwcMmaWarp) {
@@ -930,7 +975,7 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                     break;
                 tc::mma_commit(&tfull[buf]);
             }
-            if (*aborted && issued)
+            if (issued)
                 drain_mmas(&drain_bar);
         }
         __syncwarp();

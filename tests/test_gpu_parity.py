@@ -143,6 +143,8 @@ INTER_CASES = [  # (B, N, d, include_self)
     (4900, 70, 64, True),
     # two chunks of vectors over two d tiles, the second ragged (a sample's tiles share its Gs)
     (2500, 45, 200, True),
+    # a last chunk of 21 and of 20 vectors (its last 16-byte column group half padding)
+    (4900, 52, 64, False), (4900, 83, 64, True),
 ]
 
 KERNELS = {"auto": sdi.INTERACT_KERNEL_AUTO, "cuda-core": sdi.INTERACT_KERNEL_CUDA_CORE}
