@@ -198,8 +198,8 @@ sort_hist_kernel(int bits, int passes, const int64_t *__restrict__ indices, Tabl
     const int tid = threadIdx.x;
     const int64_t tau = blockIdx.x >> 1;
     const int half = blockIdx.x & 1;
-    if (tid == 0)
-        find_tile(tau, T, w.tile_base, w.tstart, ti);
+    if (tid < 32)
+        find_tile_warp(tau, T, w.tile_base, w.tstart, ti);
     for (int i = tid; i < kMaxPasses * kRadix; i += kSortThreads)
         (&h[0][0])[i] = 0;
     __syncthreads();
@@ -321,14 +321,21 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
     __shared__ uint32_t tdig[kRadix];  // exclusive prefix of the tile's digit counts
     __shared__ uint32_t gbase[kRadix];
     __shared__ uint32_t wsum[8];
+    __shared__ uint16_t srank[kItems][kSortThreads];  // each key's rank among its warp's keys of its digit
     __shared__ TileInfo ti;
     __shared__ uint32_t tau_s;
     __shared__ int timed_out;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        tau_s = atomicAdd(&w.tile_ctr[pass], 1u);
-        find_tile(tau_s, T, w.tile_base, w.tstart, ti);
-        timed_out = 0;
+    if (tid < 32) {
+        uint32_t tau = 0;
+        if (lane == 0)
+            tau = atomicAdd(&w.tile_ctr[pass], 1u);
+        tau = __shfl_sync(0xffffffffu, tau, 0);
+        find_tile_warp(tau, T, w.tile_base, w.tstart, ti);
+        if (lane == 0) {
+            tau_s = tau;
+            timed_out = 0;
+        }
     }
     for (int i = tid; i < 8 * kRadix; i += kSortThreads)
         (&whist[0][0])[i] = 0;
@@ -346,7 +353,7 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
     uint32_t *vals_out = w.vals[pass & 1];
     const int64_t R = ts.rows[ti.t];
 
-    uint32_t key[kItems], rank[kItems];  // values are read at the local scatter
+    uint32_t key[kItems];  // values are read at the local scatter
     const uint32_t wbase = ti.lo + warp * (kTile / 8);
 #pragma unroll
     for (int i = 0; i < kItems; i++) {
@@ -372,7 +379,7 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
         if (valid && lane == __ffs(peers) - 1)
             whist[warp][digit] += __popc(peers);
         __syncwarp();
-        rank[i] = r;
+        srank[i][tid] = (uint16_t)r;
     }
     __syncthreads();
     // per digit: exclusive prefix across warps and the tile's total
@@ -411,32 +418,49 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
         const uint32_t j = wbase + i * 32 + lane;
         if (j < ti.hi) {
             const uint32_t digit = (key[i] >> shift) & mask;
-            const uint32_t lp = tdig[digit] + whist[warp][digit] + rank[i];
+            const uint32_t lp = tdig[digit] + whist[warp][digit] + srank[i][tid];
             skey[lp] = key[i];
             sval[lp] = pass == 0 ? j : vals_in[j];
         }
     }
     // look back over the tiles before this one in the table (after the local
-    // scatter, so that they have had the longest time to publish)
+    // scatter, so that they have had the longest time to publish): the words
+    // of up to 4 tiles k, k - 1, .. (none before the table's first) are read
+    // at once and taken in order, down to an inclusive count; a word not yet
+    // written is read again, with those before it
     if (tid < radix) {
         uint32_t excl = 0;
         if (!first) {
             uint32_t k = tau - 1;
             int spins = 0;
             for (;;) {
-                const uint64_t v = load_status(stat + (size_t)k * kRadix + tid);
-                const uint32_t kind = (uint32_t)(v >> 32);
-                if (kind == 0u) {
-                    if (++spins > spin_limit) {
-                        timed_out = 1;
-                        break;
+                const uint32_t m = k - t0 + 1 < 4u ? k - t0 + 1 : 4u;
+                uint64_t v[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++)
+                    v[q] = (uint32_t)q < m ? load_status(stat + (size_t)(k - q) * kRadix + tid) : 0ull;
+                bool done = false, stalled = false;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    if (done || stalled || (uint32_t)q >= m)
+                        continue;
+                    const uint32_t kind = (uint32_t)(v[q] >> 32);
+                    if (kind == 0u) {
+                        stalled = true;
+                        continue;
                     }
-                    continue;
+                    excl += (uint32_t)v[q];
+                    if (kind == kInclusive || k == t0)
+                        done = true;
+                    else
+                        k--;
                 }
-                excl += (uint32_t)v;
-                if (kind == kInclusive || k == t0)
+                if (done)
                     break;
-                k--;
+                if (stalled && ++spins > spin_limit) {
+                    timed_out = 1;
+                    break;
+                }
             }
             store_status(stat + (size_t)tau * kRadix + tid, kInclusive, excl + total);
         }
@@ -470,8 +494,8 @@ seg_count_kernel(int T, int final_buf, BwdPtrs w)
     __shared__ TileInfo ti;
     __shared__ uint32_t wc[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0)
-        find_tile(blockIdx.x, T, w.tile_base, w.tstart, ti);
+    if (tid < 32)
+        find_tile_warp(blockIdx.x, T, w.tile_base, w.tstart, ti);
     __syncthreads();
     if (!ti.valid)
         return;

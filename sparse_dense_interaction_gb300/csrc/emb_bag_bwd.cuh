@@ -61,6 +61,40 @@ __device__ __forceinline__ void find_tile(int64_t tau, int T, const uint32_t *ti
     ti.valid = 1;
 }
 
+// The same by the 32 lanes of one warp (all of them call it; lane 0 writes
+// ti).  For fewer than 32 tables every lane loads one table's first tile and
+// first position at once, and a ballot counts the tables that start at or
+// before tau (the tile's table is the last of them): one round trip to
+// memory instead of a binary search's chain of loads.
+__device__ __forceinline__ void find_tile_warp(int64_t tau, int T, const uint32_t *tile_base,
+                                               const uint32_t *tstart, TileInfo &ti)
+{
+    const int lane = threadIdx.x & 31;
+    if (T >= 32) {
+        if (lane == 0)
+            find_tile(tau, T, tile_base, tstart, ti);
+        return;
+    }
+    const uint32_t tb = lane <= T ? tile_base[lane] : 0xffffffffu;
+    const uint32_t ts = lane <= T ? tstart[lane] : 0u;
+    const int n = __popc(__ballot_sync(0xffffffffu, lane < T && (int64_t)tb <= tau));
+    const int t = n > 0 ? n - 1 : 0;
+    const uint32_t total = __shfl_sync(0xffffffffu, tb, T);
+    const uint32_t tbt = __shfl_sync(0xffffffffu, tb, t);
+    const uint32_t lo = __shfl_sync(0xffffffffu, ts, t);
+    const uint32_t end = __shfl_sync(0xffffffffu, ts, t + 1);
+    if (lane == 0) {
+        if (tau >= (int64_t)total) {
+            ti.valid = 0;
+            return;
+        }
+        ti.t = t;
+        ti.lo = lo + (uint32_t)(tau - tbt) * kTile;
+        ti.hi = ti.lo + kTile < end ? ti.lo + kTile : end;
+        ti.valid = 1;
+    }
+}
+
 // A sorted position starts a run when it is the first lookup of its table
 // or its row differs from the previous sorted row.
 __device__ __forceinline__ bool run_starts(const uint32_t *skey, uint32_t j, uint32_t table_start)

@@ -167,8 +167,8 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     if (*w.sort_failed)  // the coalescing gave up a wait: its results are invalid, update nothing
         return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0)
-        find_tile(blockIdx.x, a.T, w.tile_base, w.tstart, ti);
+    if (tid < 32)
+        find_tile_warp(blockIdx.x, a.T, w.tile_base, w.tstart, ti);
     if (tid < NS)
         cbase[tid] = 0;
     __syncthreads();
