@@ -291,6 +291,7 @@ sort_digit_scan_kernel(int passes, int T, BwdPtrs w)
 constexpr uint32_t kAggregate = 1u;  // the tile's own count of the digit
 constexpr uint32_t kInclusive = 2u;  // count of the digit in this and all earlier tiles of the table
 constexpr int kSpinLimit = 1 << 20;  // default polls of one word before a wait gives up (about a second)
+constexpr int kFewDigits = 16;       // distinct digits among a warp's items below which a match is cheaper
 
 __device__ __forceinline__ void store_status(uint64_t *p, uint32_t kind, uint32_t count)
 {
@@ -365,12 +366,31 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
             key[i] = valid ? keys_in[j] : 0u;
     }
     // stable rank within the warp: items in position order (i, then lane)
+    bool few = false;
 #pragma unroll
     for (int i = 0; i < kItems; i++) {
         const uint32_t j = wbase + i * 32 + lane;
         const bool valid = j < ti.hi;
         const uint32_t digit = valid ? (key[i] >> shift) & mask : (uint32_t)kRadix;
-        const unsigned peers = __match_any_sync(0xffffffffu, digit);
+        // lanes with the same digit: a match instruction, whose cost grows with the number
+        // of distinct digits among the lanes, while the previous item had few of them, else
+        // one ballot per digit bit (a constant cost; the lanes past the end of a table's
+        // last tile match none of the others)
+        unsigned peers;
+        if (few) {
+            peers = __match_any_sync(0xffffffffu, digit);
+        } else {
+            peers = __ballot_sync(0xffffffffu, valid);
+            if (!valid)
+                peers = ~peers;
+#pragma unroll
+            for (int b = 0; b < kRadixBits; b++) {
+                const bool bit = (digit >> b) & 1u;
+                const unsigned m = __ballot_sync(0xffffffffu, bit);
+                peers &= bit ? m : ~m;
+            }
+        }
+        few = __popc(__ballot_sync(0xffffffffu, lane == __ffs(peers) - 1)) <= kFewDigits;
         const uint32_t before = __popc(peers & ((1u << lane) - 1u));
         uint32_t r = 0;
         if (valid)
