@@ -58,7 +58,7 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.seg_off = take(n4 + 4);
     L.status[0] = take((size_t)kRadix * L.ntiles_max * 8);
     L.status[1] = take((size_t)kRadix * L.ntiles_max * 8);
-    L.tile_ctr = take(((size_t)kMaxPasses + 1) * 4);  // the passes' tile counters, then the sort-failed word
+    L.tile_ctr = take(((size_t)kMaxPasses + 2) * 4);  // the passes' tile counters, the sort-failed word, the value kind
     L.tile_hist = take((size_t)L.ntiles_max * 2 * kMaxPasses * kRadix * 4);
     L.counts = take((size_t)kMaxPasses * T * kRadix * 4);
     L.tstart = take(((size_t)T + 1) * 4);
@@ -81,7 +81,7 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
 
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nnz, BwdPtrs w,
-                uint32_t first_tile, int32_t *err)
+                uint32_t first_tile, uint32_t vals_bags, int32_t *err)
 {
     __shared__ int64_t start[DLRM_MAX_TABLES + 1];
     for (int t = threadIdx.x; t <= T; t += blockDim.x)
@@ -117,6 +117,8 @@ bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t n
         w.tile_ctr[threadIdx.x] = first_tile;  // 0 unless a test leaves the first tiles unclaimed
     if (threadIdx.x == kMaxPasses)
         *w.sort_failed = 0;
+    if (threadIdx.x == kMaxPasses + 1)
+        *w.vals_bags = vals_bags;
 }
 
 // ------------------------------------------------------------- bag ids ---
@@ -348,6 +350,7 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
     w.status[(pass + 1) & 1][(size_t)tau * kRadix + tid] = 0;
     const uint32_t mask = (1u << nbits) - 1u;
     const int radix = 1 << nbits;
+    const bool first_vals_bags = pass == 0 && *w.vals_bags != 0u;  // the first pass's values: bags or positions
     const uint32_t *keys_in = w.keys[(pass + 1) & 1];
     const uint32_t *vals_in = w.vals[(pass + 1) & 1];
     uint32_t *keys_out = w.keys[pass & 1];
@@ -440,7 +443,7 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
             const uint32_t digit = (key[i] >> shift) & mask;
             const uint32_t lp = tdig[digit] + whist[warp][digit] + srank[i][tid];
             skey[lp] = key[i];
-            sval[lp] = pass == 0 ? j : vals_in[j];
+            sval[lp] = pass == 0 ? (first_vals_bags ? w.bag_of[j] : j) : vals_in[j];
         }
     }
     // look back over the tiles before this one in the table (after the local
@@ -646,6 +649,7 @@ static BwdPtrs bind_workspace(int T, int64_t nnz, int d, void *workspace)
     w.status[1] = reinterpret_cast<uint64_t *>(base + L.status[1]);
     w.tile_ctr = reinterpret_cast<uint32_t *>(base + L.tile_ctr);
     w.sort_failed = w.tile_ctr + kMaxPasses;
+    w.vals_bags = w.tile_ctr + kMaxPasses + 1;
     w.tile_hist = reinterpret_cast<uint32_t *>(base + L.tile_hist);
     w.counts = reinterpret_cast<uint32_t *>(base + L.counts);
     w.tstart = reinterpret_cast<uint32_t *>(base + L.tstart);
@@ -692,7 +696,10 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
 
     const WaitHooks hooks = wait_hooks(kSpinLimit, 0);
     int s;
-    bwd_prep_kernel<<<1, 256, 0, st>>>(offsets, T, B, nnz, w, hooks.sort_first_tile, err);
+    // without a view the sort carries each lookup's bag (read in position order in the first pass),
+    // so the reduce need not gather it by position; the view keeps the positions
+    const uint32_t vals_bags = view ? 0u : 1u;
+    bwd_prep_kernel<<<1, 256, 0, st>>>(offsets, T, B, nnz, w, hooks.sort_first_tile, vals_bags, err);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;

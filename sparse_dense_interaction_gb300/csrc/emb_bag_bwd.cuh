@@ -25,6 +25,7 @@ struct BwdPtrs {
     uint32_t *keys[2], *vals[2], *bag_of, *uniq_row, *seg_off, *tile_ctr, *tile_hist, *counts, *tstart, *tile_base,
         *tile_count, *tile_ubase, *chunk_flags, *chunk_tail_u, *block_flags;
     uint32_t *sort_failed;  // set by a radix pass whose wait ran out: the reduce then updates nothing
+    uint32_t *vals_bags;    // 1: the sort carried each lookup's bag (no view asked for); 0: its position
     int32_t *uniq_table;
     uint64_t *status[2];  // look-back words of the radix passes, by tile and digit
     float *head, *tail, *block_sum;

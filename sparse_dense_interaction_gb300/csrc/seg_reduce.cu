@@ -188,7 +188,9 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     TT *wtab = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t]));
     const int64_t rows_t = a.tables.rows[t];
 
-    // A. stage rows and bag ids (8 lookups per thread in flight)
+    // A. stage rows and bag ids (8 lookups per thread in flight); the sort carried the bag ids
+    // unless the coalescing was asked for its view (then the positions, whose bags are looked up)
+    const bool vals_bags = *w.vals_bags != 0u;
     for (int r0 = 0; r0 < PER; r0 += 8) {
         uint32_t pos[8];
 #pragma unroll
@@ -204,7 +206,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
         for (int r = 0; r < 8; r++) {
             const uint32_t i = (uint32_t)(r0 + r) * kReduceThreads + tid;
             if (i < n) {
-                uint32_t b = w.bag_of[pos[r]];
+                uint32_t b = vals_bags ? pos[r] : w.bag_of[pos[r]];
                 if ((int64_t)b >= a.B) {
                     raise_flag(a.err, DLRM_FLAG_BAD_OFFSETS);
                     b = kNoBag;
