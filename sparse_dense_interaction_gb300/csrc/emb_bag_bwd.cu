@@ -149,6 +149,7 @@ bag_ids_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nn
         if (bag > last)
             o = nnz + 1;
         const int64_t start = __shfl_sync(0xffffffffu, o, 0);
+        const uint32_t bid = (uint32_t)((g0 + lane) % B);  // this lane's bag within its table, once per group
         // warp-uniform trip count: every lane takes part in every shuffle
         for (int64_t p0 = start; p0 < end; p0 += 32) {
             const int64_t p = p0 + lane;
@@ -160,8 +161,9 @@ bag_ids_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nn
                 if (cand < 32 && oc <= p)
                     l = cand;
             }
+            const uint32_t b = __shfl_sync(0xffffffffu, bid, l);
             if (p < end)
-                bag_of[p] = (uint32_t)((g0 + l) % B);
+                bag_of[p] = b;
         }
     }
 }
