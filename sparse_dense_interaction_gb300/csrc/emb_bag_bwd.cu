@@ -526,10 +526,25 @@ seg_count_kernel(int T, int final_buf, BwdPtrs w)
         return;
     const uint32_t *skey = w.keys[final_buf];
     const uint32_t ts = w.tstart[ti.t];
+    // a sorted position starts a run when it is its table's first or its row differs from
+    // the previous sorted row; all of the thread's keys are in flight at once, and a key's
+    // predecessor comes from the lane before (lane 0 reads its own)
+    constexpr int PER = kTile / 256;
+    uint32_t k[PER], kp[PER];
+#pragma unroll
+    for (int i = 0; i < PER; i++) {
+        const uint32_t j = ti.lo + (uint32_t)i * 256 + tid;
+        const bool in = j < ti.hi;
+        k[i] = in ? skey[j] : 0u;
+        kp[i] = (in && lane == 0 && j != ts) ? skey[j - 1] : 0u;
+    }
     uint32_t count = 0;
-    for (uint32_t jb = ti.lo; jb < ti.hi; jb += 256) {
-        const uint32_t j = jb + tid;
-        const bool start = j < ti.hi && run_starts(skey, j, ts);
+#pragma unroll
+    for (int i = 0; i < PER; i++) {
+        const uint32_t j = ti.lo + (uint32_t)i * 256 + tid;
+        const uint32_t up = __shfl_up_sync(0xffffffffu, k[i], 1);
+        const uint32_t prev = lane == 0 ? kp[i] : up;
+        const bool start = j < ti.hi && (j == ts || k[i] != prev);
         count += __popc(__ballot_sync(0xffffffffu, start));
     }
     if (lane == 0)

@@ -96,13 +96,6 @@ __device__ __forceinline__ void find_tile_warp(int64_t tau, int T, const uint32_
     }
 }
 
-// A sorted position starts a run when it is the first lookup of its table
-// or its row differs from the previous sorted row.
-__device__ __forceinline__ bool run_starts(const uint32_t *skey, uint32_t j, uint32_t table_start)
-{
-    return j == table_start || skey[j] != skey[j - 1];
-}
-
 // Optimizers of the update: plain SGD, or row-wise AdaGrad (one fp32
 // accumulator per row: s' = s + mean(g^2), w' = w - lr g / (sqrt(s') + eps)).
 constexpr int kOptSgd = 0, kOptAdagrad = 1;
