@@ -52,6 +52,21 @@ int check_bwd_sgd_args(void *const *tables, const int64_t *rows, int T, int d, i
                        int64_t dpts, float lr, const float *grad_rows, int64_t grad_rows_cap, const void *workspace,
                        size_t workspace_bytes, TableSet &ts);
 
+// Table t and sample b of bag `bag` (table-major: bag = t * B + b), by a 32-bit
+// division when every bag index fits in 32 bits (`small`, fixed per launch), as
+// it does for all but gigantic batches; 64 bits otherwise.
+__device__ __forceinline__ void bag_table_sample(int64_t bag, int64_t B, bool small, int &t, int64_t &b)
+{
+    if (small) {
+        const uint32_t q = (uint32_t)bag / (uint32_t)B;
+        t = (int)q;
+        b = bag - (int64_t)q * B;
+    } else {
+        t = (int)(bag / B);
+        b = bag - (int64_t)t * B;
+    }
+}
+
 __device__ __forceinline__ void raise_flag(int32_t *flag, int bits)
 {
     if (flag)

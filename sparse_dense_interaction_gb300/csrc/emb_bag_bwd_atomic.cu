@@ -74,13 +74,15 @@ emb_bag_bwd_atomic_kernel(TableSet ts, int T, int d, const int64_t *__restrict__
     const int gl = lane % G, grp = lane / G;
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (grp * G));
     const int64_t nbags = (int64_t)T * B;
+    const bool small = nbags <= 0xffffffffll;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const float step = -lr;
 
     for (int64_t bag = warp * GPW + grp; bag < nbags; bag += nwarps * GPW) {
-        const int t = (int)(bag / B);
-        const int64_t b = bag - (int64_t)t * B;
+        int t;
+        int64_t b;
+        bag_table_sample(bag, B, small, t, b);
         int64_t k0 = offsets[bag];
         int64_t k1 = offsets[bag + 1];
         if (k0 < 0 || k1 < k0 || k1 > nnz) {

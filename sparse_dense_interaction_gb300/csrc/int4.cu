@@ -94,14 +94,16 @@ emb_bag_fwd_int4_kernel(TableSet ts, int T, int d, int64_t rb, const int64_t *__
     const int grp = lane / G;
     const unsigned gmask = (G == 32) ? 0xffffffffu : (((1u << G) - 1u) << (grp * G));
     const int64_t nbags = (int64_t)T * B;
+    const bool small = nbags <= 0xffffffffll;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const bool on = 16 * gl < d;  // this lane owns codes 16 gl .. 16 gl + 15
     const bool pair_params = d % 16 == 0;  // scale and bias 8-byte aligned: one load
 
     for (int64_t bag = warp * GPW + grp; bag < nbags; bag += nwarps * GPW) {
-        const int t = (int)(bag / B);
-        const int64_t b = bag - (int64_t)t * B;
+        int t;
+        int64_t b;
+        bag_table_sample(bag, B, small, t, b);
         int64_t k0 = offsets[bag];
         int64_t k1 = offsets[bag + 1];
         if (k0 < 0 || k1 < k0 || k1 > nnz) {
