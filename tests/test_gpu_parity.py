@@ -55,6 +55,10 @@ FWD_CASES = {
     "d3-f32-scalar": dict(name="tiny", B=64, rows=[40, 50, 60], d=3),
     "d512-f32": dict(name="tiny", B=40, rows=[300, 20], d=512),
     "d8-f16": dict(name="multi-hot", B=50, rows=[300, 20], d=8),
+    # half rows of 12 and 10 chunks (8 lanes of two chunks, some idle) and of 9 (16 lanes)
+    "d96-f16": dict(name="multi-hot", B=120, rows=[3000, 70], d=96),
+    "d80-bf16": dict(name="multi-hot", B=120, rows=[3000, 70], d=80, dtype="bf16"),
+    "d72-f16": dict(name="multi-hot", B=120, rows=[3000, 70], d=72),
 }
 
 
