@@ -143,8 +143,10 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
 // fp32 values of every gradient row (piece c of lane l covers elements
 // (c*G + l)*VEC ..), U lookups in flight per stream.  With the update on, the
 // table rows of runs that start PD steps ahead are prefetched into L2, so the
-// read-modify-write at a run's end finds its row there.
-template <typename TT, int VEC, int G, int C, int U, int PD>
+// read-modify-write at a run's end finds its row there.  FULL: d is a whole
+// number of passes of G*C*VEC elements, so every piece lies inside the row and
+// the gathers test only that the lookup has a bag.
+template <typename TT, int VEC, int G, int C, int U, int PD, bool FULL>
 __global__ void __launch_bounds__(kReduceThreads, 4)
 seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
 {
@@ -377,7 +379,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
 #pragma unroll
                 for (int c = 0; c < C; c++) {
                     g[u][c] = V::zero();
-                    if (b != kNoBag && on[c])
+                    if (b != kNoBag && (FULL || on[c]))
                         g[u][c] = V::load(src + c * G * VEC);
                 }
             }
@@ -596,7 +598,10 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
 template <typename TT, int VEC, int G, int C, int U, int PD>
 static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaStream_t st)
 {
-    seg_reduce_kernel<TT, VEC, G, C, U, PD><<<(unsigned)grid, kReduceThreads, 0, st>>>(a, w);
+    if (a.d % (G * C * VEC) == 0)
+        seg_reduce_kernel<TT, VEC, G, C, U, PD, true><<<(unsigned)grid, kReduceThreads, 0, st>>>(a, w);
+    else
+        seg_reduce_kernel<TT, VEC, G, C, U, PD, false><<<(unsigned)grid, kReduceThreads, 0, st>>>(a, w);
     count_launch(st);
     int s = launch_status();
     if (s != DLRM_OK)
