@@ -162,7 +162,10 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     constexpr uint32_t kNoBag = 0x7fffffffu;       // bag word: no valid bag
     static_assert(NS <= 32 && CW % 32 == 0, "chunk geometry");
 
-    __shared__ uint2 skb[kTile];  // sorted row, bag of the lookup | kStart at run starts
+    // sorted row, bag of the lookup | kStart at run starts; lookup i at sk(i): one spare entry
+    // after each chunk, so the two 16-lane streams of a warp read different banks
+    __shared__ uint2 skb[kTile + NS];
+    auto sk = [](uint32_t i) { return i + i / CW; };
     __shared__ uint32_t cbase[NS];
     __shared__ TileInfo ti;
     __shared__ uint32_t key_before, key_after;
@@ -200,7 +203,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
             const uint32_t i = (uint32_t)(r0 + r) * kReduceThreads + tid;
             pos[r] = 0;
             if (i < n) {
-                skb[i].x = skey[lo + i];
+                skb[sk(i)].x = skey[lo + i];
                 pos[r] = sval[lo + i];
             }
         }
@@ -213,7 +216,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                     raise_flag(a.err, DLRM_FLAG_BAD_OFFSETS);
                     b = kNoBag;
                 }
-                skb[i].y = b;
+                skb[sk(i)].y = b;
             }
         }
     }
@@ -223,9 +226,9 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
         const uint32_t i = (uint32_t)r * kReduceThreads + tid;
         bool st = false;
         if (i < n) {
-            st = lo + i == ts || skb[i].x != (i == 0 ? key_before : skb[i - 1].x);
+            st = lo + i == ts || skb[sk(i)].x != (i == 0 ? key_before : skb[sk(i - 1)].x);
             if (st)
-                skb[i].y |= kStart;
+                skb[sk(i)].y |= kStart;
         }
         const unsigned bal = __ballot_sync(0xffffffffu, st);
         if (lane == 0 && bal)
@@ -234,7 +237,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     // pad the tile to a whole number of steps with lookups that contribute
     // nothing and start no run, so the walk below needs no bounds checks
     if (tid < (int)((U - n % U) % U))  // n is then below kTile, a multiple of U
-        skb[n + tid] = make_uint2(0u, kNoBag);
+        skb[sk(n + tid)] = make_uint2(0u, kNoBag);
     __syncthreads();
     if (warp == 0) {
         const uint32_t v = lane < NS ? cbase[lane] : 0u;
@@ -262,8 +265,9 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
             w.chunk_flags[ch] = 0;
         return;
     }
-    const bool carry_in = !(skb[c0].y & kStart);
-    const bool carry_out = c1 < n ? !(skb[c1].y & kStart) : (ti.hi < te && key_after == skb[n - 1].x);
+    const bool carry_in = !(skb[sk(c0)].y & kStart);
+    const bool carry_out = c1 < n ? !(skb[sk(c1)].y & kStart) : (ti.hi < te && key_after == skb[sk(n - 1)].x);
+    const uint2 *skc = skb + sidx;  // this chunk's lookups: skc[p] is lookup p (p in c0 .. c1e)
     const uint32_t ub = cbase[sidx];
     uint32_t flags = 0;
 
@@ -355,7 +359,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                 for (int u = 0; u < U; u++) {
                     const uint32_t q = p0 + PD * U + u;
                     if (q < c1) {
-                        const uint2 kb = skb[q];
+                        const uint2 kb = skc[q];
                         if ((kb.y & kStart) && (int64_t)kb.x < rows_t) {
                             const TT *wr = wtab + (int64_t)kb.x * a.d + eb + gl * VEC;
 #pragma unroll
@@ -372,7 +376,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
             uint32_t starts = 0;  // bit u: a run starts at p0 + u
 #pragma unroll
             for (int u = 0; u < U; u++) {
-                const uint32_t by = skb[p0 + u].y;
+                const uint32_t by = skc[p0 + u].y;
                 starts |= (by >> 31) << u;
                 const uint32_t b = by & ~kStart;
                 const float *src = reinterpret_cast<const float *>(dpt_bytes + (uint64_t)b * dpss_bytes);
@@ -389,7 +393,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                     if (p0 + u > c0)
                         flush(false);
                     cur_carry = false;
-                    cur_row = skb[p0 + u].x;
+                    cur_row = skc[p0 + u].x;
                     cur_start = lo + p0 + u;
                     cur_u = ub + nseg;
                     nseg++;
