@@ -391,8 +391,9 @@ interact_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
 //   A = Z^T in tensor memory (lane m holds z_k[m], k = 0 .. F-1, e0 first),
 //   B = Gs = G + G^T in shared memory (row n holds Gs[n][k]; a self pair
 //     counts twice),
-// split hi + lo on both sides, three MMAs per K step (hi.hi + lo.hi +
-// hi.lo).  F <= 32: one K tile.  Bulk tensor copies bring the unit's raw rows
+// split hi + lo on both sides (hi = x truncated to TF32, lo = x - hi exactly,
+// which the MMA reads truncated in turn: what the three MMAs per K step,
+// hi.hi + lo.hi + hi.lo, leave out stays below 3 * 2^-20 of |z||g|).  F <= 32: one K tile.  Bulk tensor copies bring the unit's raw rows
 // of Z (unswizzled, one row per vector), 4-byte asynchronous copies its pair
 // gradients (a row of dy need not be 16-byte aligned); the converters write A
 // into tensor memory (no shared-memory write) and Gs into shared memory
@@ -529,8 +530,8 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
                 float z = 0.f;
                 if (k < F && a < bx)
                     z = *reinterpret_cast<const float *>(raw + (k == 0 ? e0off : (uint32_t)(k - 1) * rs) + a * 4);
-                zh[k] = tc::tf32_round(z);
-                zl[k] = tc::tf32_round(z - zh[k]);
+                zh[k] = tc::tf32_trunc(z);
+                zl[k] = z - zh[k];  // exact; the MMA reads it truncated to TF32
             }
             const float *dyp = reinterpret_cast<const float *>(raw + dyoff);
 #pragma unroll
@@ -538,8 +539,8 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
                 float v = gidx[e] >= 0 ? dyp[gidx[e]] : 0.f;
                 if (gself[e])
                     v *= 2.f;  // a self pair counts in G and in G^T
-                gh[e] = tc::tf32_round(v);
-                gl[e] = tc::tf32_round(v - gh[e]);
+                gh[e] = tc::tf32_trunc(v);
+                gl[e] = v - gh[e];
             }
             tc::mbar_arrive(&empty[slot]);  // the raw slot has been read
             if (av > 0 && !tc::mbar_wait(&aempty[as], (av - 1) & 1, aborted))
@@ -669,8 +670,9 @@ interact_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
 //   A = Z^T in tensor memory (lane m holds z_k[m], k = 0 .. F-1, e0 first),
 //   B = Gs = G + G^T in shared memory (row n holds Gs[n][k]; a self pair
 //     counts twice),
-// split hi + lo on both sides, three MMAs per K step (hi.hi + lo.hi +
-// hi.lo).  K runs in chunks of 32 vectors: a bulk tensor copy brings the
+// split hi + lo on both sides (hi = x truncated to TF32, lo = x - hi exactly,
+// which the MMA reads truncated in turn: what the three MMAs per K step,
+// hi.hi + lo.hi + hi.lo, leave out stays below 3 * 2^-20 of |z||g|).  K runs in chunks of 32 vectors: a bulk tensor copy brings the
 // chunk's 32 raw rows of Z (unswizzled; the box starts one row before the
 // chunk, so for the first chunk its row 0 reads as zero and e0 comes in a row
 // of its own), 4-byte asynchronous copies bring the unit's pair gradients
@@ -867,8 +869,8 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                     if (a < bx && 32 * c + r < F)
                         z = *reinterpret_cast<const float *>(raw + (c == 0 && r == 0 ? 32 * rs : (uint32_t)r * rs) +
                                                              a * 4);
-                    zh[r] = tc::tf32_round(z);
-                    zl[r] = tc::tf32_round(z - zh[r]);
+                    zh[r] = tc::tf32_trunc(z);
+                    zl[r] = z - zh[r];  // exact; the MMA reads it truncated to TF32
                 }
                 tc::mbar_arrive(&zempty[zs]);
                 if (av > 0 && !tc::mbar_wait(&aempty[as], (av - 1) & 1, aborted)) {
@@ -914,8 +916,8 @@ interact_bwd_tc_chunked_kernel(const __grid_constant__ CUtensorMap map_emb,
                     float h[4], l[4];
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
-                        h[j] = tc::tf32_round(v[j]);
-                        l[j] = tc::tf32_round(v[j] - h[j]);
+                        h[j] = tc::tf32_trunc(v[j]);
+                        l[j] = v[j] - h[j];
                     }
                     const uint32_t o = sw128(n, (k0 & 31) >> 2);
                     *reinterpret_cast<float4 *>(bh + o) = make_float4(h[0], h[1], h[2], h[3]);
