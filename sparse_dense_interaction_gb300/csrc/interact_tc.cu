@@ -85,7 +85,8 @@ __device__ __forceinline__ void drain_mmas(uint64_t *bar)
 //     tile's e0 rows (one box, so every box starts on a 1024-byte boundary);
 //   A (tensor memory, written by the converters): lane s Fb + i - 1 = pooled
 //     row i, lane s Fb + N = e0 of sample s, as [t | 2 lo] along K with
-//     lo = x - t rounded to TF32, so D = t t'^T + 2 lo t'^T.
+//     lo = x - t exactly (the MMA reads 2 lo truncated to TF32), so
+//     D = t t'^T + 2 lo t'^T.
 // For two vectors u, v of a sample with lanes a, b and B rows a', b',
 // (D[a][b'] + D[b][a']) / 2 = t_u.t_v + lo_u.t_v + t_u.lo_v: the product to
 // about 2^-20 of |u||v| (lo.lo', below 2^-20, is dropped).  e0's B row is
@@ -267,7 +268,7 @@ interact_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_emb, const __grid
 #pragma unroll
                 for (int k = 0; k < 32; k++) {
                     tv[k] = tc::tf32_trunc(v[k]);
-                    lv[k] = tc::tf32_round(2.f * (v[k] - tv[k]));
+                    lv[k] = 2.f * (v[k] - tv[k]);  // exact; the MMA reads it truncated to TF32
                 }
                 // A slot `as` is free once the MMAs of item it - kFwdAS are done, which the B slot
                 // of that item signals (NS > kFwdAS, so that phase cannot have been passed)
