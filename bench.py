@@ -718,10 +718,11 @@ def e2e_measure(args, st, torch, sdi, stream, dev):
     """Same metric through the public API, every step's inputs copied from
     pinned host memory and its results read back, pipelined as a training
     loop would be: two device buffer sets; the inputs of step i+1 are copied
-    on a copy stream while step i computes, and the results of step i are read
-    back while step i+1 computes.  Events order every copy against the steps
-    that use the buffer.  The timed region covers K steps from the first input
-    copy to the last result read back."""
+    on one copy stream while step i computes, and the results of step i are
+    read back on another while step i+1 computes (the two directions overlap).
+    Events order every copy against the steps that use the buffer.  The timed
+    region covers K steps from the first input copy to the last result read
+    back."""
     c = st.cfg
     K = args.e2e_steps or max(3, args.steps // 2)
     names_in = ["offsets", "indices"] + (["e0", "dy"] if st.inter else ["dpooled"])
@@ -736,19 +737,19 @@ def e2e_measure(args, st, torch, sdi, stream, dev):
                  for n in names_out} for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
-    copy = torch.cuda.Stream(dev)
+    copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     in_ready = [torch.cuda.Event() for _ in range(2)]
     step_done = [torch.cuda.Event() for _ in range(2)]
     out_done = [torch.cuda.Event() for _ in range(2)]
 
     def load(i):  # inputs of step i into set i % 2, once step i - 2 no longer reads it
         k = i % 2
-        with torch.cuda.stream(copy):
+        with torch.cuda.stream(copy_in):
             if i >= 2:
-                copy.wait_event(step_done[k])
+                copy_in.wait_event(step_done[k])
             for n in names_in:
                 sets[k][n].copy_(host_in[n], non_blocking=True)
-            in_ready[k].record(copy)
+            in_ready[k].record(copy_in)
 
     def step(i):  # step i on set i % 2, then its results read back
         k = i % 2
@@ -759,11 +760,11 @@ def e2e_measure(args, st, torch, sdi, stream, dev):
             setattr(st, n, t)
         st.run()
         step_done[k].record(stream)
-        with torch.cuda.stream(copy):
-            copy.wait_event(step_done[k])
+        with torch.cuda.stream(copy_out):
+            copy_out.wait_event(step_done[k])
             for n in names_out:
                 host_out[k][n].copy_(sets[k][n], non_blocking=True)
-            out_done[k].record(copy)
+            out_done[k].record(copy_out)
 
     def loop(n):
         load(0)
@@ -778,7 +779,8 @@ def e2e_measure(args, st, torch, sdi, stream, dev):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    copy.wait_event(a)
+    copy_in.wait_event(a)
+    copy_out.wait_event(a)
     loop(K)
     b.record(stream)
     torch.cuda.synchronize()
@@ -788,7 +790,7 @@ def e2e_measure(args, st, torch, sdi, stream, dev):
     return {"value": c["B"] / (ms / 1e3), "unit": "samples/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "pipelined": "inputs of step i+1 copied while step i computes; results of step i read back "
-                         "while step i+1 computes (two buffer sets, copy stream)"}
+                         "while step i+1 computes (two buffer sets, one copy stream per direction)"}
 
 
 def main():
