@@ -150,20 +150,22 @@ bag_ids_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nn
             o = nnz + 1;
         const int64_t start = __shfl_sync(0xffffffffu, o, 0);
         const uint32_t bid = (uint32_t)((g0 + lane) % B);  // this lane's bag within its table, once per group
+        // positions relative to the group's first one fit in 32 bits (nnz <= 2^31): 32-bit shuffles
+        // and compares in the search (lanes past the last bag never match)
+        const uint32_t orel = o <= nnz ? (uint32_t)(o - start) : 0xffffffffu;
+        const uint32_t n = (uint32_t)(end - start);
         // warp-uniform trip count: every lane takes part in every shuffle
-        for (int64_t p0 = start; p0 < end; p0 += 32) {
-            const int64_t p = p0 + lane;
+        for (uint32_t q0 = 0; q0 < n; q0 += 32) {
+            const uint32_t q = q0 + lane;
             int l = 0;
 #pragma unroll
-            for (int step = 16; step > 0; step >>= 1) {
-                const int cand = l + step;
-                const int64_t oc = __shfl_sync(0xffffffffu, o, cand & 31);
-                if (cand < 32 && oc <= p)
-                    l = cand;
+            for (int step = 16; step > 0; step >>= 1) {  // l + step <= 31
+                if (__shfl_sync(0xffffffffu, orel, l + step) <= q)
+                    l += step;
             }
             const uint32_t b = __shfl_sync(0xffffffffu, bid, l);
-            if (p < end)
-                bag_of[p] = b;
+            if (q < n)
+                bag_of[start + q] = b;
         }
     }
 }
