@@ -59,7 +59,7 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.status[0] = take((size_t)kRadix * L.ntiles_max * 8);
     L.status[1] = take((size_t)kRadix * L.ntiles_max * 8);
     L.tile_ctr = take(((size_t)kMaxPasses + 2) * 4);  // the passes' tile counters, the sort-failed word, the value kind
-    L.tile_hist = take((size_t)L.ntiles_max * 2 * kMaxPasses * kRadix * 4);
+    L.tile_hist = take((size_t)L.ntiles_max * kMaxPasses * kRadix * 4);
     L.counts = take((size_t)kMaxPasses * T * kRadix * 4);
     L.tstart = take(((size_t)T + 1) * 4);
     L.tile_base = take(((size_t)T + 1) * 4);
@@ -187,44 +187,43 @@ __host__ __device__ __forceinline__ int pass_bits(int bits, int passes, int p)
     return bits / passes + (p < bits % passes ? 1 : 0);
 }
 
-// Digit counts of every pass from one read of the indices, per half tile
-// (two CTAs per tile), written to the tile's row of counts.  A table's digit
+// Digit counts of every pass from one read of the indices, one CTA of 512
+// threads per tile (8 indices per thread in flight), written to the tile's row
+// of counts.  A table's digit
 // histogram does not depend on the order of its keys, so all passes are
 // counted here; the digit scan below sums the rows of the table's tiles, and
 // each pass finds the counts of the tiles before its own by looking back.
 // Also clears the look-back words of pass 0 and flags indices out of range.
-constexpr int kHistItems = kItems / 2;
-__global__ void __launch_bounds__(kSortThreads)
+__global__ void __launch_bounds__(2 * kSortThreads)
 sort_hist_kernel(int bits, int passes, const int64_t *__restrict__ indices, TableSet ts, int T, BwdPtrs w,
                  int32_t *err)
 {
-    static_assert(kSortThreads == kRadix, "one thread per digit");
+    constexpr int kThreads = 2 * kSortThreads;  // 512: one CTA per tile, 8 indices per thread in flight
     __shared__ uint32_t h[kMaxPasses][kRadix];
     __shared__ TileInfo ti;
     const int tid = threadIdx.x;
-    const int64_t tau = blockIdx.x >> 1;
-    const int half = blockIdx.x & 1;
+    const int64_t tau = blockIdx.x;
     if (tid < 32)
         find_tile_warp(tau, T, w.tile_base, w.tstart, ti);
-    for (int i = tid; i < kMaxPasses * kRadix; i += kSortThreads)
+    for (int i = tid; i < kMaxPasses * kRadix; i += kThreads)
         (&h[0][0])[i] = 0;
     __syncthreads();
     if (!ti.valid)
         return;
-    if (tid < kRadix / 2)
-        w.status[0][(size_t)tau * kRadix + half * (kRadix / 2) + tid] = 0;
+    if (tid < kRadix)
+        w.status[0][(size_t)tau * kRadix + tid] = 0;
     const int64_t R = ts.rows[ti.t];
-    const uint32_t lo = ti.lo + half * (kTile / 2);
-    uint32_t key[kHistItems];
+    const uint32_t lo = ti.lo;
+    uint32_t key[kTile / kThreads];
 #pragma unroll
-    for (int i = 0; i < kHistItems; i++) {
-        const uint32_t j = lo + i * kSortThreads + tid;
+    for (int i = 0; i < kTile / kThreads; i++) {
+        const uint32_t j = lo + i * kThreads + tid;
         key[i] = j < ti.hi ? pass0_key(indices, j, R) : 0u;
     }
     bool oob = false;
 #pragma unroll
-    for (int i = 0; i < kHistItems; i++) {
-        if (lo + i * kSortThreads + tid < ti.hi) {
+    for (int i = 0; i < kTile / kThreads; i++) {
+        if (lo + i * kThreads + tid < ti.hi) {
             oob |= key[i] == kSentinel;
             int shift = 0;
             for (int p = 0; p < passes; p++) {
@@ -238,11 +237,11 @@ sort_hist_kernel(int bits, int passes, const int64_t *__restrict__ indices, Tabl
         raise_flag(err, DLRM_FLAG_INDEX_OOB);
     __syncthreads();
     uint32_t *row = w.tile_hist + ((size_t)blockIdx.x * kMaxPasses) * kRadix;
-    for (int p = 0; p < passes; p++)
-        row[p * kRadix + tid] = h[p][tid];
+    for (int i = tid; i < passes * kRadix; i += kThreads)
+        row[i] = (&h[0][0])[i];
 }
 
-// One CTA per (pass, table): sums the digit counts of the table's half tiles
+// One CTA per (pass, table): sums the digit counts of the table's tiles
 // (four groups of kRadix threads, one thread per digit, each over every
 // fourth row) and scans them into the start position of each digit's keys in
 // the table's sorted range.
@@ -254,9 +253,9 @@ sort_digit_scan_kernel(int passes, int T, BwdPtrs w)
     __shared__ uint32_t wsum[kRadix / 32];
     const int p = blockIdx.x / T, t = blockIdx.x % T;
     const int tid = threadIdx.x, dg = tid % kRadix, g = tid / kRadix, lane = tid & 31, warp = tid >> 5;
-    const uint32_t h0 = 2 * w.tile_base[t], h1 = 2 * w.tile_base[t + 1];
+    const uint32_t h0 = w.tile_base[t], h1 = w.tile_base[t + 1];
     const uint32_t *col = w.tile_hist + (size_t)p * kRadix + dg;
-    constexpr size_t kRow = (size_t)kMaxPasses * kRadix;  // words per half tile
+    constexpr size_t kRow = (size_t)kMaxPasses * kRadix;  // words per tile
     uint32_t c = 0;
     uint32_t hb = h0 + g;
     for (; hb + 3 * kScanGroups < h1; hb += 4 * kScanGroups) {
@@ -736,7 +735,7 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
             return s;
     }
     const int64_t grid = L.ntiles_max;
-    sort_hist_kernel<<<(unsigned)(2 * grid), kSortThreads, 0, st>>>(bits, passes, indices, ts, T, w, err);
+    sort_hist_kernel<<<(unsigned)grid, 2 * kSortThreads, 0, st>>>(bits, passes, indices, ts, T, w, err);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
