@@ -100,6 +100,35 @@ def test_adagrad_matches_oracle(case):
     _check(cfg, host, s0, offsets, indices, dp, lr, tables, state, grad, view, case)
 
 
+@pytest.mark.parametrize("case", list(CASES))
+def test_adagrad_without_a_view_gives_the_same_bits(case):
+    # the sort carries bags instead of positions when no view is asked for; the sums, the
+    # accumulators and the rows must equal those of the view path bit for bit
+    c, kind = CASES[case]
+    c = dict(c)
+    cfg = W.make_config(c.pop("name"), **c)
+    host = W.tables_host(cfg)
+    offsets, indices = W.make_indices(cfg)
+    dp = _t(W.make_dpooled(cfg))
+    s0 = _state0(cfg, kind)
+    nnz = indices.size
+    out = []
+    for want_view in (True, False):
+        tables = W.tables_to_device(host, cfg["dtype"])
+        state = [_t(s) for s in s0]
+        ws = torch.empty(sdi.dlrm_emb_bag_bwd_workspace_size(cfg["T"], cfg["B"], nnz, cfg["d"]),
+                         dtype=torch.uint8, device=DEV)
+        grad = torch.full((nnz, cfg["d"]), float("nan"), device=DEV)
+        sdi.dlrm_emb_bag_bwd_adagrad(tables, state, _t(offsets), _t(indices), cfg["B"], dp, 0.05, EPS, ws,
+                                     grad_rows=grad, want_view=want_view)
+        out.append((tables, state, grad))
+    (t1, s1, g1), (t2, s2, g2) = out
+    np.testing.assert_array_equal(g2.cpu().numpy().view(np.uint32), g1.cpu().numpy().view(np.uint32))
+    for t in range(cfg["T"]):
+        np.testing.assert_array_equal(device_table_bits(t2[t]), device_table_bits(t1[t]))
+        np.testing.assert_array_equal(s2[t].cpu().numpy().view(np.uint32), s1[t].cpu().numpy().view(np.uint32))
+
+
 def test_adagrad_long_runs_cross_chunks():
     # almost every lookup of table 0 hits row 7: one run over many reduce
     # chunks and sort tiles, combined by the finalize (which applies AdaGrad)

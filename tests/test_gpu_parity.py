@@ -288,10 +288,12 @@ BWD_CASES = {
     "d17-scalar": dict(name="multi-hot", B=300, rows=[100, 200], d=17),
     "d3-f32": dict(name="tiny", B=64, rows=[40, 50, 60], d=3),
     "d512-f32": dict(name="tiny", B=300, rows=[300, 20], d=512, bag=("poisson", 5.0, 0, 12)),
+    # 40 tables: the sort's tiles find their table by a search, not by one warp's ballot
+    "40-tables": dict(name="multi-hot", B=200, T=40, rows=[3000] * 40),
 }
 
 
-def _run_bwd(cfg, host, offsets, indices, dp, lr, grad_cap=None):
+def _run_bwd(cfg, host, offsets, indices, dp, lr, grad_cap=None, want_view=True):
     tables = W.tables_to_device(host, cfg["dtype"])
     nnz = indices.size
     ws = torch.empty(sdi.dlrm_emb_bag_bwd_workspace_size(cfg["T"], cfg["B"], nnz, cfg["d"]),
@@ -299,9 +301,29 @@ def _run_bwd(cfg, host, offsets, indices, dp, lr, grad_cap=None):
     grad = None if grad_cap is None else torch.full((grad_cap, cfg["d"]), float("nan"), device=DEV)
     flag = _flag()
     view = sdi.dlrm_emb_bag_bwd_sgd(tables, _t(offsets), _t(indices), cfg["B"], _t(dp), lr, ws,
-                                    grad_rows=grad, err_flag=flag, want_view=True)
+                                    grad_rows=grad, err_flag=flag, want_view=want_view)
     status = sdi.dlrm_read_error(flag)
     return tables, grad, view, status
+
+
+@pytest.mark.parametrize("case", list(BWD_CASES))
+def test_emb_bag_bwd_sgd_without_a_view_gives_the_same_bits(case):
+    # without a view the sort carries each lookup's bag instead of its position; the runs are
+    # summed in the same sorted order either way, so tables and coalesced gradients must agree
+    # bit for bit with the view path, which the oracle parity test checks
+    c = dict(BWD_CASES[case])
+    cfg = W.make_config(c.pop("name"), **c)
+    host = W.tables_host(cfg)
+    offsets, indices = W.make_indices(cfg)
+    dp = W.make_dpooled(cfg)
+    nnz = indices.size
+    t_view, g_view, _, s_view = _run_bwd(cfg, host, offsets, indices, dp, 0.05, grad_cap=nnz)
+    t_bags, g_bags, view, s_bags = _run_bwd(cfg, host, offsets, indices, dp, 0.05, grad_cap=nnz, want_view=False)
+    assert view is None
+    assert s_view == 0 and s_bags == 0
+    np.testing.assert_array_equal(g_bags.cpu().numpy().view(np.uint32), g_view.cpu().numpy().view(np.uint32))
+    for t in range(cfg["T"]):
+        np.testing.assert_array_equal(device_table_bits(t_bags[t]), device_table_bits(t_view[t]))
 
 
 def _check_coalesce(view, co, nnz):
