@@ -456,27 +456,36 @@ class KernelProfiler:
 BWD_KERNELS_PREFIX = ["bwd_prep", "bag_ids"]
 
 
-def coalesce_kernel_names(passes):
+NUMBER_KERNELS = ["seg_count", "seg_scan"]  # number the unique keys: for a view or gradient rows
+
+
+def coalesce_kernel_names(passes, numbered=False):
     names = list(BWD_KERNELS_PREFIX) + ["sort_hist", "sort_digit_scan"]
     names += [f"sort_pass[{p}]" for p in range(passes)]
-    return names + ["seg_count", "seg_scan"]
+    return names + (NUMBER_KERNELS if numbered else [])
 
 
 REDUCE_KERNELS = ["seg_reduce", "seg_block_sum", "seg_finalize"]
 
 
-def bwd_kernel_names(passes):
-    return coalesce_kernel_names(passes) + REDUCE_KERNELS
+def reduce_kernel_names(grad_rows):
+    # the reduce numbers the unique keys first when it is given gradient rows (no view is asked
+    # for here, so the coalescing leaves them unnumbered)
+    return (NUMBER_KERNELS if grad_rows else []) + REDUCE_KERNELS
 
 
-def kernel_name(call, k, passes):
+def bwd_kernel_names(passes, grad_rows=False):
+    return coalesce_kernel_names(passes) + reduce_kernel_names(grad_rows)
+
+
+def kernel_name(call, k, passes, grad_rows=False):
     """Name of the k-th kernel that a library call launched."""
     if call == "emb_bag_bwd":
-        return bwd_kernel_names(passes)[k]
+        return bwd_kernel_names(passes, grad_rows)[k]
     if call == "coalesce":
         return coalesce_kernel_names(passes)[k]
     if call == "reduce_sgd":
-        return REDUCE_KERNELS[k]
+        return reduce_kernel_names(grad_rows)[k]
     if call == "emb_bag_interact_fwd" and k > 0:  # the two-kernel path of the fused call
         return "interact_fwd"
     return call
@@ -501,9 +510,10 @@ def algorithmic_bytes(cfg, st):
         out["emb_bag_interact_fwd"] = out["emb_bag_fwd"] + B * d * 4 + B * width * 4
         out["interact_fwd"] = B * (T + 1) * d * 4 + B * width * 4
         out["interact_bwd"] = B * (T + 1) * d * 4 + B * width * 4 + B * (T + 1) * d * 4
-    # the reduce + update kernel: sorted keys and positions, bag ids, the
-    # pooled gradient, and one read-modify-write of every unique row
-    out["seg_reduce"] = st.nnz * 12 + nb * d * 4 + 2 * uniq * d * es
+    # the reduce + update kernel: the sorted keys and the bags the sort carried
+    # (no view is asked for), the pooled gradient, and one read-modify-write of
+    # every unique row
+    out["seg_reduce"] = st.nnz * 8 + nb * d * 4 + 2 * uniq * d * es
     # the whole backward (coalescing + reduce, or the atomic update): the
     # indices and offsets, the pooled gradient, one read-modify-write of every
     # unique row (the sort's own passes are not compulsory traffic)
@@ -517,7 +527,7 @@ def algorithmic_bytes(cfg, st):
 
 def stage_times(kernel_ms, passes):
     """Per-stage milliseconds of one step from the per-kernel times."""
-    coal = sum(kernel_ms.get(k, 0.0) for k in coalesce_kernel_names(passes))
+    coal = sum(kernel_ms.get(k, 0.0) for k in coalesce_kernel_names(passes, numbered=True))
     red = sum(kernel_ms.get(k, 0.0) for k in REDUCE_KERNELS)
     out = {"lookup": kernel_ms.get("emb_bag_fwd"), "coalesce": coal or None, "reduce": red or None}
     if "emb_bag_bwd_atomic" in kernel_ms:
@@ -552,7 +562,8 @@ def measure_target(name, args, dev, update="sorted"):
     torch.cuda.synchronize()
     ms_step = a.elapsed_time(b) / K
     passes = (max(1, int(np.ceil(np.log2(max(cfg["rows"]))))) + 7) // 8
-    kernel_ms = {kernel_name(c, k, passes): float(np.mean(v)) for (c, k), v in prof.per_kernel_ms().items()}
+    kernel_ms = {kernel_name(c, k, passes, st.grad is not None): float(np.mean(v))
+                 for (c, k), v in prof.per_kernel_ms().items()}
     alg, uniq = algorithmic_bytes(cfg, st)
     peak, _ = measured_peaks()
     stages = {}
@@ -652,7 +663,7 @@ def run_ours(args):
     passes = (bits + 7) // 8
     names = {}
     for (call, k) in per:
-        names[(call, k)] = kernel_name(call, k, passes)
+        names[(call, k)] = kernel_name(call, k, passes, st.grad is not None)
     kernel_ms = {names[key]: float(np.mean(v)) for key, v in per.items()}
     alg, uniq = algorithmic_bytes(cfg, st)
     peak, peak_kind = measured_peaks()

@@ -30,7 +30,8 @@ namespace dlrm {
 
 struct BwdLayout {
     size_t keys[2], vals[2], bag_of, uniq_table, uniq_row, seg_off, status[2], tile_ctr, tile_hist, counts, tstart, tile_base,
-        tile_count, tile_ubase, chunk_flags, chunk_tail_u, head, tail, block_flags, block_sum, num_unique, total;
+        tile_count, tile_ubase, chunk_flags, chunk_tail_u, chunk_tail_row, chunk_tail_t, head, tail, block_flags,
+        block_sum, num_unique, total;
     int64_t ntiles_max, nchunks_max;
 };
 
@@ -58,7 +59,7 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.seg_off = take(n4 + 4);
     L.status[0] = take((size_t)kRadix * L.ntiles_max * 8);
     L.status[1] = take((size_t)kRadix * L.ntiles_max * 8);
-    L.tile_ctr = take(((size_t)kMaxPasses + 2) * 4);  // the passes' tile counters, the sort-failed word, the value kind
+    L.tile_ctr = take(((size_t)kMaxPasses + 3) * 4);  // the passes' tile counters, sort failed, value kind, ids ready
     L.tile_hist = take((size_t)L.ntiles_max * kMaxPasses * kRadix * 4);
     L.counts = take((size_t)kMaxPasses * T * kRadix * 4);
     L.tstart = take(((size_t)T + 1) * 4);
@@ -67,6 +68,8 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.tile_ubase = take((size_t)L.ntiles_max * 4);
     L.chunk_flags = take((size_t)L.nchunks_max * 4);
     L.chunk_tail_u = take((size_t)L.nchunks_max * 4);
+    L.chunk_tail_row = take((size_t)L.nchunks_max * 4);
+    L.chunk_tail_t = take((size_t)L.nchunks_max * 4);
     L.head = take((size_t)L.nchunks_max * d * 4);
     L.tail = take((size_t)L.nchunks_max * d * 4);
     const int64_t nblocks = L.nchunks_max / kFinalizeBlock + 1;
@@ -119,6 +122,8 @@ bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t n
         *w.sort_failed = 0;
     if (threadIdx.x == kMaxPasses + 1)
         *w.vals_bags = vals_bags;
+    if (threadIdx.x == kMaxPasses + 2)
+        *w.ids_ready = 0;  // until the unique keys are numbered
 }
 
 // ------------------------------------------------------------- bag ids ---
@@ -617,6 +622,7 @@ seg_scan_kernel(int T, int64_t nnz, BwdPtrs w)
     if (tid == 0) {
         *w.num_unique = carry;
         w.seg_off[carry] = (uint32_t)nnz;
+        *w.ids_ready = 1;
     }
 }
 
@@ -668,6 +674,7 @@ static BwdPtrs bind_workspace(int T, int64_t nnz, int d, void *workspace)
     w.tile_ctr = reinterpret_cast<uint32_t *>(base + L.tile_ctr);
     w.sort_failed = w.tile_ctr + kMaxPasses;
     w.vals_bags = w.tile_ctr + kMaxPasses + 1;
+    w.ids_ready = w.tile_ctr + kMaxPasses + 2;
     w.tile_hist = reinterpret_cast<uint32_t *>(base + L.tile_hist);
     w.counts = reinterpret_cast<uint32_t *>(base + L.counts);
     w.tstart = reinterpret_cast<uint32_t *>(base + L.tstart);
@@ -676,6 +683,8 @@ static BwdPtrs bind_workspace(int T, int64_t nnz, int d, void *workspace)
     w.tile_ubase = reinterpret_cast<uint32_t *>(base + L.tile_ubase);
     w.chunk_flags = reinterpret_cast<uint32_t *>(base + L.chunk_flags);
     w.chunk_tail_u = reinterpret_cast<uint32_t *>(base + L.chunk_tail_u);
+    w.chunk_tail_row = reinterpret_cast<uint32_t *>(base + L.chunk_tail_row);
+    w.chunk_tail_t = reinterpret_cast<int32_t *>(base + L.chunk_tail_t);
     w.head = reinterpret_cast<float *>(base + L.head);
     w.tail = reinterpret_cast<float *>(base + L.tail);
     w.block_flags = reinterpret_cast<uint32_t *>(base + L.block_flags);
@@ -693,6 +702,21 @@ static void sort_plan(const TableSet &ts, int T, int &bits, int &passes, int &fi
     bits = row_bits(ts, T);
     passes = (bits + kRadixBits - 1) / kRadixBits;
     final_buf = (passes - 1) & 1;
+}
+
+// Numbers the unique keys of a coalescing (their runs' starts counted per
+// tile, then scanned): the view's arrays and the gradient rows are indexed by
+// these numbers; the update itself does not need them.
+static int launch_number_keys(int T, int64_t nnz, int final_buf, int64_t grid, BwdPtrs w, cudaStream_t st)
+{
+    seg_count_kernel<<<(unsigned)grid, 256, 0, st>>>(T, final_buf, w);
+    count_launch(st);
+    int s = launch_status();
+    if (s != DLRM_OK)
+        return s;
+    seg_scan_kernel<<<1, 1024, 0, st>>>(T, nnz, w);
+    count_launch(st);
+    return launch_status();
 }
 
 int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, const int64_t *indices,
@@ -753,13 +777,9 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
             return s;
         shift += nb;
     }
-    seg_count_kernel<<<(unsigned)grid, 256, 0, st>>>(T, final_buf, w);
-    count_launch(st);
-    if ((s = launch_status()) != DLRM_OK)
-        return s;
-    seg_scan_kernel<<<1, 1024, 0, st>>>(T, nnz, w);
-    count_launch(st);
-    return launch_status();
+    if (!view)  // the unique keys are numbered for a view, or by the reduce for gradient rows
+        return DLRM_OK;
+    return launch_number_keys(T, nnz, final_buf, grid, w, st);
 }
 
 int launch_reduce_sgd(const TableSet &ts, int T, int d, int dtype, int64_t nnz, int64_t B, const float *dpooled,
@@ -772,6 +792,11 @@ int launch_reduce_sgd(const TableSet &ts, int T, int d, int dtype, int64_t nnz, 
     BwdPtrs w = bind_workspace(T, nnz, d, workspace);
     int bits, passes, final_buf;
     sort_plan(ts, T, bits, passes, final_buf);
+    if (grad_rows) {  // gradient rows are indexed by the unique keys' numbers
+        const int s = launch_number_keys(T, nnz, final_buf, L.ntiles_max, w, st);
+        if (s != DLRM_OK)
+            return s;
+    }
     ReduceArgs a;
     a.tables = ts;
     a.T = T;

@@ -26,6 +26,9 @@ struct BwdPtrs {
         *tile_count, *tile_ubase, *chunk_flags, *chunk_tail_u, *block_flags;
     uint32_t *sort_failed;  // set by a radix pass whose wait ran out: the reduce then updates nothing
     uint32_t *vals_bags;    // 1: the sort carried each lookup's bag (no view asked for); 0: its position
+    uint32_t *ids_ready;    // 1: the unique keys are numbered (tile_ubase, num_unique): a view or gradient rows
+    uint32_t *chunk_tail_row;  // row and table of the run that leaves each chunk (read by the finalize)
+    int32_t *chunk_tail_t;
     int32_t *uniq_table;
     uint64_t *status[2];  // look-back words of the radix passes, by tile and digit
     float *head, *tail, *block_sum;

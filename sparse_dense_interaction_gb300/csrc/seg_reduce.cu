@@ -171,6 +171,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
     __shared__ uint32_t key_before, key_after;
     if (*w.sort_failed)  // the coalescing gave up a wait: its results are invalid, update nothing
         return;
+    const bool ids = *w.ids_ready != 0u;  // the unique keys are numbered: write the view's arrays
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < 32)
         find_tile_warp(blockIdx.x, a.T, w.tile_base, w.tstart, ti);
@@ -249,7 +250,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                 incl += x;
         }
         if (lane < NS)
-            cbase[lane] = w.tile_ubase[blockIdx.x] + incl - v;
+            cbase[lane] = (ids ? w.tile_ubase[blockIdx.x] : 0u) + incl - v;
     }
     __syncthreads();
 
@@ -293,7 +294,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                         V::store(w.head + ch * a.d + eb + (c * G + gl) * VEC, acc[c]);
                 flags |= kHasHead | ((last && carry_out) ? 0u : kHeadEnds);
             } else {
-                if (eb == 0 && gl == 0) {
+                if (ids && eb == 0 && gl == 0) {
                     w.uniq_table[cur_u] = t;
                     w.uniq_row[cur_u] = cur_row;
                     w.seg_off[cur_u] = cur_start;
@@ -304,8 +305,11 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                         if (on[c])
                             V::store(w.tail + ch * a.d + eb + (c * G + gl) * VEC, acc[c]);
                     flags |= kHasTail;
-                    if (eb == 0 && gl == 0)
-                        w.chunk_tail_u[ch] = cur_u;
+                    if (eb == 0 && gl == 0) {
+                        w.chunk_tail_row[ch] = cur_row;
+                        w.chunk_tail_t[ch] = t;
+                        w.chunk_tail_u[ch] = cur_u;  // meaningful when the keys are numbered
+                    }
                 } else {
                     if (a.grad_rows) {
                         if ((int64_t)cur_u < a.grad_cap) {
@@ -505,9 +509,9 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
     for (size_t ch = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); ch < nch; ch += nwarps) {
         if (!(w.chunk_flags[ch] & kHasTail))
             continue;
-        const uint32_t u = w.chunk_tail_u[ch];
-        const uint32_t row = w.uniq_row[u];
-        const int t = w.uniq_table[u];
+        const uint32_t row = w.chunk_tail_row[ch];
+        const int t = w.chunk_tail_t[ch];
+        const uint32_t u = a.grad_rows ? w.chunk_tail_u[ch] : 0u;  // gradient rows: the keys are numbered
         // chunks up to the next block boundary, one by one
         const size_t c1 = ch + 1;
         const size_t bound = ((c1 + kFinalizeBlock - 1) / kFinalizeBlock) * kFinalizeBlock;
