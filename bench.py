@@ -674,7 +674,9 @@ def run_ours(args):
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
-            traffic = json.load(f).get(cfg["name"], {}).get(rl_kernel)
+            # the captures are of the SGD kernels; other optimizers have their own entry, or none
+            key = cfg["name"] if st.optimizer == "sgd" else f'{cfg["name"]}+{st.optimizer}'
+            traffic = json.load(f).get(key, {}).get(rl_kernel)
     roofline = {"kernel": rl_kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "algorithmic_bytes": alg[rl_kernel], "peak_source": peak_kind,

@@ -376,7 +376,11 @@ int dlrm_emb_bag_reduce_sgd(void *const *tables, const int64_t *rows, int T, int
  *
  *   state[t][r] <- s' = state[t][r] + (1/d) sum_e g_u[e]^2
  *   tables[t][r][e] <- tables[t][r][e] - lr * g_u[e] / (sqrt(s') + eps)
- *                      (one fused multiply-add, one rounding to the table type)
+ *
+ * The row update rounds as dlrm_emb_bag_bwd_sgd's does, with the step
+ * lr / (sqrt(s') + eps) in place of lr: fp32 and fp16 rows by one L2
+ * reduction of the rounded step (two roundings), bf16 rows by one fused
+ * multiply-add and one rounding.  The accumulator is rounded once (fp32).
  *
  * state   host array of T device pointers, each fp32 [rows[t]], 4-byte
  *         aligned: the accumulators, updated in place for touched rows only

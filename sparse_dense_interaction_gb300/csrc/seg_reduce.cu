@@ -15,12 +15,13 @@
 //     adds; the table rows of runs starting a step ahead are prefetched into
 //     L2.  The kernel is kept lean (at most 64 registers, so 4 CTAs of 8
 //     warps share an SM and hide the latency of the row gathers); when a run
-//     ends its table row is read, updated (SGD: w - lr*g; AdaGrad: the row's
+//     ends its table row is updated once (SGD: w - lr*g; AdaGrad: the row's
 //     sum of squares reduced over the stream, the accumulator updated once,
-//     w - lr*g/(sqrt(s')+eps); one rounding to the table type) and written,
-//     once per unique row.  Runs that cross a chunk boundary leave partial
-//     sums, which two small kernels combine in chunk order (block sums of 32
-//     chunks, then the run's owner), so results are deterministic.
+//     w - lr*g/(sqrt(s')+eps)): fp32 and fp16 rows by an L2 reduction of the
+//     rounded step, bf16 rows read, updated and written back.  Runs that
+//     cross a chunk boundary leave partial sums, which two small kernels
+//     combine in chunk order (block sums of 32 chunks, then the run's owner),
+//     so results are deterministic.
 #include <type_traits>
 
 #include "emb_bag_bwd.cuh"
@@ -81,9 +82,10 @@ struct RowChunk {
     }
 };
 
-// The SGD update of fp32 and fp16 rows as one reduction performed in L2: the
-// step -lr*g is computed in fp32, rounded to the table type and added to the
-// row (rounded again); nothing waits for the row.  Each unique row receives
+// The update of fp32 and fp16 rows as one reduction performed in L2: the
+// step -lr*g (AdaGrad: lr / (sqrt(s') + eps) in place of lr) is computed in
+// fp32, rounded to the table type and added to the row (rounded again);
+// nothing waits for the row.  Each unique row receives
 // one such update per launch (its run's whole sum), so the result does not
 // depend on timing.  bf16 rows keep the read-modify-write (one rounding):
 // their 8-bit significand leaves too little room for two.
@@ -343,7 +345,7 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                         for (int c = 0; c < C; c++)
                             if (on[c]) {
                                 TT *wp = wtab + (int64_t)cur_row * a.d + eb + (c * G + gl) * VEC;
-                                if (RedUpdate<TT, VEC>::kUse && !adagrad)
+                                if (RedUpdate<TT, VEC>::kUse)
                                     RedUpdate<TT, VEC>::apply(wp, acc[c], step);
                                 else
                                     RC::store(wp, RC::sgd(RC::load(wp), acc[c], step));
@@ -365,11 +367,13 @@ seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
                     if (q < c1) {
                         const uint2 kb = skc[q];
                         if ((kb.y & kStart) && (int64_t)kb.x < rows_t) {
-                            const TT *wr = wtab + (int64_t)kb.x * a.d + eb + gl * VEC;
+                            if (!RedUpdate<TT, VEC>::kUse) {  // rows updated in L2 are not read here
+                                const TT *wr = wtab + (int64_t)kb.x * a.d + eb + gl * VEC;
 #pragma unroll
-                            for (int c = 0; c < C; c++)
-                                if (on[c])
-                                    prefetch_l2(wr + c * G * VEC);
+                                for (int c = 0; c < C; c++)
+                                    if (on[c])
+                                        prefetch_l2(wr + c * G * VEC);
+                            }
                             if (adagrad && gl == 0)
                                 prefetch_l2(a.state.ptr[t] + kb.x);
                         }
@@ -574,7 +578,10 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
                 }
                 if (in_table && a.lr != 0.f) {
                     TT *wp = static_cast<TT *>(const_cast<void *>(a.tables.ptr[t])) + (int64_t)row * a.d + e;
-                    RowChunk<TT, VEC>::store(wp, RowChunk<TT, VEC>::sgd(RowChunk<TT, VEC>::load(wp), acc[nb], step));
+                    if (RedUpdate<TT, VEC>::kUse)
+                        RedUpdate<TT, VEC>::apply(wp, acc[nb], step);
+                    else
+                        RowChunk<TT, VEC>::store(wp, RowChunk<TT, VEC>::sgd(RowChunk<TT, VEC>::load(wp), acc[nb], step));
                 }
             }
             continue;
