@@ -461,9 +461,14 @@ BWD_KERNELS_PREFIX = ["bwd_prep", "bag_ids"]
 NUMBER_KERNELS = ["seg_count", "seg_scan"]  # number the unique keys: for a view or gradient rows
 
 
-def coalesce_kernel_names(passes, numbered=False):
-    names = list(BWD_KERNELS_PREFIX) + ["sort_hist", "sort_digit_scan"]
-    names += [f"sort_pass[{p}]" for p in range(passes)]
+def coalesce_kernel_names(plan, numbered=False):
+    """Kernels of one coalescing; ``plan`` = (LSD passes, MSD bucket sort used), as the
+    library reports it (with the bucket sort the first pass sorts by the top digit and the
+    later passes return at once)."""
+    passes, msd = plan
+    names = list(BWD_KERNELS_PREFIX) + ["sort_hist", "sort_digit_scan", "sort_pass[0]"]
+    names += ["bucket_sort"] if msd else []
+    names += [f"sort_pass[{p}]" for p in range(1, passes)]
     return names + (NUMBER_KERNELS if numbered else [])
 
 
@@ -476,16 +481,16 @@ def reduce_kernel_names(grad_rows):
     return (NUMBER_KERNELS if grad_rows else []) + REDUCE_KERNELS
 
 
-def bwd_kernel_names(passes, grad_rows=False):
-    return coalesce_kernel_names(passes) + reduce_kernel_names(grad_rows)
+def bwd_kernel_names(plan, grad_rows=False):
+    return coalesce_kernel_names(plan) + reduce_kernel_names(grad_rows)
 
 
-def kernel_name(call, k, passes, grad_rows=False):
+def kernel_name(call, k, plan, grad_rows=False):
     """Name of the k-th kernel that a library call launched."""
     if call == "emb_bag_bwd":
-        return bwd_kernel_names(passes, grad_rows)[k]
+        return bwd_kernel_names(plan, grad_rows)[k]
     if call == "coalesce":
-        return coalesce_kernel_names(passes)[k]
+        return coalesce_kernel_names(plan)[k]
     if call == "reduce_sgd":
         return reduce_kernel_names(grad_rows)[k]
     if call == "emb_bag_interact_fwd" and k > 0:  # the two-kernel path of the fused call
@@ -527,9 +532,9 @@ def algorithmic_bytes(cfg, st):
     return out, uniq
 
 
-def stage_times(kernel_ms, passes):
+def stage_times(kernel_ms, plan):
     """Per-stage milliseconds of one step from the per-kernel times."""
-    coal = sum(kernel_ms.get(k, 0.0) for k in coalesce_kernel_names(passes, numbered=True))
+    coal = sum(kernel_ms.get(k, 0.0) for k in coalesce_kernel_names(plan, numbered=True))
     red = sum(kernel_ms.get(k, 0.0) for k in REDUCE_KERNELS)
     out = {"lookup": kernel_ms.get("emb_bag_fwd"), "coalesce": coal or None, "reduce": red or None}
     if "emb_bag_bwd_atomic" in kernel_ms:
@@ -563,13 +568,13 @@ def measure_target(name, args, dev, update="sorted"):
     b.record(stream)
     torch.cuda.synchronize()
     ms_step = a.elapsed_time(b) / K
-    passes = (max(1, int(np.ceil(np.log2(max(cfg["rows"]))))) + 7) // 8
-    kernel_ms = {kernel_name(c, k, passes, st.grad is not None): float(np.mean(v))
+    plan = sdi.dlrm_emb_bag_sort_plan(cfg["rows"], st.nnz)
+    kernel_ms = {kernel_name(c, k, plan, st.grad is not None): float(np.mean(v))
                  for (c, k), v in prof.per_kernel_ms().items()}
     alg, uniq = algorithmic_bytes(cfg, st)
     peak, _ = measured_peaks()
     stages = {}
-    for stage, ms in stage_times(kernel_ms, passes).items():
+    for stage, ms in stage_times(kernel_ms, plan).items():
         if ms is None:
             continue
         nbytes = {"lookup": alg["emb_bag_fwd"], "reduce": alg["seg_reduce"], "backward": alg["backward"]}.get(stage)
@@ -685,11 +690,10 @@ def run_ours(args):
 
     # per-kernel times (events on the launch stream) and the roofline
     per = prof.per_kernel_ms()
-    bits = max(1, int(np.ceil(np.log2(max(cfg["rows"])))))
-    passes = (bits + 7) // 8
+    plan = sdi.dlrm_emb_bag_sort_plan(cfg["rows"], st.nnz)
     names = {}
     for (call, k) in per:
-        names[(call, k)] = kernel_name(call, k, passes, st.grad is not None)
+        names[(call, k)] = kernel_name(call, k, plan, st.grad is not None)
     kernel_ms = {names[key]: float(np.mean(v)) for key, v in per.items()}
     alg, uniq = algorithmic_bytes(cfg, st)
     peak, peak_kind = measured_peaks()

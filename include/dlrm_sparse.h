@@ -266,6 +266,21 @@ typedef struct dlrm_coalesced_view {
 size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d);
 
 /*
+ * The coalescing's sort for these sizes (host only, no device work): into
+ * *passes the number of LSD radix passes over the row bits (1 to 4, digits of
+ * at most 8 bits), into *msd 1 when the sort instead orders the keys by the
+ * top 8 row bits in one pass and then sorts each table's 256 buckets in
+ * shared memory (rows of 17 bits or more, every table above half the
+ * largest power of two, and 256 to 2560 keys per bucket on average), else 0.
+ * The LSD passes are launched either way: when the digit counts show a bucket
+ * of more than 4096 keys the first launch sorts by the lowest digit and the
+ * LSD passes run, else they return at once.  Both orders are the same stable
+ * sort.  rows: host array of T row counts.  Returns DLRM_OK, or
+ * DLRM_ERR_INVALID_ARG for invalid sizes or null pointers.
+ */
+int dlrm_emb_bag_sort_plan(const int64_t *rows, int T, int64_t nnz, int *passes, int *msd);
+
+/*
  * Embedding-bag backward with row-wise SGD ("Notes/DLRM", section 5: the
  * tables are trained by an optimizer; plain SGD on the touched rows here).
  * Duplicate lookups are coalesced first (stable radix sort by (table, row),

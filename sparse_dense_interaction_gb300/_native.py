@@ -46,6 +46,7 @@ SIGNATURES = {
     "dlrm_get_interact_kernel": (_i32, []),
     "dlrm_set_wait_test_hooks": (_i32, [_i64, _i32, _i64]),
     "dlrm_emb_bag_bwd_workspace_size": (_sz, [_i32, _i64, _i64, _i32]),
+    "dlrm_emb_bag_sort_plan": (_i32, [_vp, _i32, _i64, _vp, _vp]),
     "dlrm_emb_bag_bwd_sgd": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _i64, _i64, _vp, _i64,
                                     _i64, _f32, _vp, _i64, _vp, _sz, ctypes.POINTER(CoalescedView),
                                     _vp, _vp]),
@@ -227,6 +228,17 @@ def dlrm_interact_bwd(e0, emb, include_self: bool, dy, de0, demb, stream=None, a
 
 def dlrm_emb_bag_bwd_workspace_size(T: int, B: int, nnz: int, d: int) -> int:
     return int(load().dlrm_emb_bag_bwd_workspace_size(T, B, nnz, d))
+
+
+def dlrm_emb_bag_sort_plan(rows, nnz: int):
+    """(LSD passes, MSD bucket sort used) of the coalescing for tables of
+    ``rows`` rows and ``nnz`` lookups (host only)."""
+    T = len(rows)
+    r = (ctypes.c_int64 * max(T, 1))(*rows)
+    passes, msd = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().dlrm_emb_bag_sort_plan(r, T, nnz, ctypes.byref(passes), ctypes.byref(msd)),
+           "dlrm_emb_bag_sort_plan")
+    return passes.value, bool(msd.value)
 
 
 def dlrm_emb_bag_bwd_sgd(tables, offsets, indices, B: int, dpooled, lr: float, workspace,

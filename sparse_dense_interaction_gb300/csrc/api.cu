@@ -89,6 +89,7 @@ int launch_emb_bag_interact_fwd(const TableSet &, int, int, int, const int64_t *
                                 const FusedShape &, int32_t *, cudaStream_t);
 bool emb_bag_bwd_vectorisable(const TableSet &, int, int, const float *, int64_t, int64_t, const float *);
 size_t emb_bag_bwd_workspace(int, int64_t, int);
+void coalesce_plan(const int64_t *, int, int64_t, int &, bool &);
 int launch_emb_bag_bwd(const TableSet &, int, int, int, const int64_t *, const int64_t *, int64_t, int64_t,
                        const float *, int64_t, int64_t, float, float *, int64_t, void *, bool,
                        dlrm_coalesced_view *, int32_t *, cudaStream_t);
@@ -344,6 +345,19 @@ size_t dlrm_emb_bag_bwd_workspace_size(int T, int64_t B, int64_t nnz, int d)
     if (T <= 0 || T > DLRM_MAX_TABLES || B < 0 || nnz < 0 || nnz > kMaxLookups || d <= 0)
         return 0;
     return emb_bag_bwd_workspace(T, nnz, d);
+}
+
+int dlrm_emb_bag_sort_plan(const int64_t *rows, int T, int64_t nnz, int *passes, int *msd)
+{
+    if (!rows || !passes || !msd || T <= 0 || T > DLRM_MAX_TABLES || nnz < 0 || nnz > kMaxLookups)
+        return DLRM_ERR_INVALID_ARG;
+    for (int t = 0; t < T; t++)
+        if (rows[t] <= 0)
+            return DLRM_ERR_INVALID_ARG;
+    bool m = false;
+    coalesce_plan(rows, T, nnz, *passes, m);
+    *msd = m ? 1 : 0;
+    return DLRM_OK;
 }
 
 }  // extern "C"

@@ -59,9 +59,10 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
     L.seg_off = take(n4 + 4);
     L.status[0] = take((size_t)kRadix * L.ntiles_max * 8);
     L.status[1] = take((size_t)kRadix * L.ntiles_max * 8);
-    L.tile_ctr = take(((size_t)kMaxPasses + 3) * 4);  // the passes' tile counters, sort failed, value kind, ids ready
-    L.tile_hist = take((size_t)L.ntiles_max * kMaxPasses * kRadix * 4);
-    L.counts = take((size_t)kMaxPasses * T * kRadix * 4);
+    // the LSD passes' and the MSD pass's tile counters, sort failed, value kind, ids ready, MSD state
+    L.tile_ctr = take(((size_t)kMaxPasses + 5) * 4);
+    L.tile_hist = take((size_t)L.ntiles_max * kSortRows * kRadix * 4);
+    L.counts = take((size_t)kSortRows * T * kRadix * 4);
     L.tstart = take(((size_t)T + 1) * 4);
     L.tile_base = take(((size_t)T + 1) * 4);
     L.tile_count = take((size_t)L.ntiles_max * 4);
@@ -84,7 +85,7 @@ BwdLayout bwd_layout(int T, int64_t nnz, int d)
 
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nnz, BwdPtrs w,
-                uint32_t first_tile, uint32_t vals_bags, int32_t *err)
+                uint32_t first_tile, uint32_t vals_bags, uint32_t msd, int32_t *err)
 {
     __shared__ int64_t start[DLRM_MAX_TABLES + 1];
     for (int t = threadIdx.x; t <= T; t += blockDim.x)
@@ -116,14 +117,16 @@ bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t n
     __syncthreads();
     for (int t = threadIdx.x; t <= T; t += blockDim.x)
         w.tstart[t] = (uint32_t)start[t];
-    if (threadIdx.x < kMaxPasses)
+    if (threadIdx.x <= kMaxPasses)
         w.tile_ctr[threadIdx.x] = first_tile;  // 0 unless a test leaves the first tiles unclaimed
-    if (threadIdx.x == kMaxPasses)
-        *w.sort_failed = 0;
     if (threadIdx.x == kMaxPasses + 1)
-        *w.vals_bags = vals_bags;
+        *w.sort_failed = 0;
     if (threadIdx.x == kMaxPasses + 2)
+        *w.vals_bags = vals_bags;
+    if (threadIdx.x == kMaxPasses + 3)
         *w.ids_ready = 0;  // until the unique keys are numbered
+    if (threadIdx.x == kMaxPasses + 4)
+        *w.msd_state = msd ? kMsdPlanned : 0u;
 }
 
 // ------------------------------------------------------------- bag ids ---
@@ -198,19 +201,21 @@ __host__ __device__ __forceinline__ int pass_bits(int bits, int passes, int p)
 // histogram does not depend on the order of its keys, so all passes are
 // counted here; the digit scan below sums the rows of the table's tiles, and
 // each pass finds the counts of the tiles before its own by looking back.
-// Also clears the look-back words of pass 0 and flags indices out of range.
+// With msd_shift >= 0 row `passes` counts the top digit (key >> msd_shift)
+// for the pass that sorts by it first.  Also clears the look-back words of
+// pass 0 and flags indices out of range.
 __global__ void __launch_bounds__(2 * kSortThreads)
-sort_hist_kernel(int bits, int passes, const int64_t *__restrict__ indices, TableSet ts, int T, BwdPtrs w,
-                 int32_t *err)
+sort_hist_kernel(int bits, int passes, int msd_shift, const int64_t *__restrict__ indices, TableSet ts, int T,
+                 BwdPtrs w, int32_t *err)
 {
     constexpr int kThreads = 2 * kSortThreads;  // 512: one CTA per tile, 8 indices per thread in flight
-    __shared__ uint32_t h[kMaxPasses][kRadix];
+    __shared__ uint32_t h[kSortRows][kRadix];
     __shared__ TileInfo ti;
     const int tid = threadIdx.x;
     const int64_t tau = blockIdx.x;
     if (tid < 32)
         find_tile_warp(tau, T, w.tile_base, w.tstart, ti);
-    for (int i = tid; i < kMaxPasses * kRadix; i += kThreads)
+    for (int i = tid; i < kSortRows * kRadix; i += kThreads)
         (&h[0][0])[i] = 0;
     __syncthreads();
     if (!ti.valid)
@@ -236,23 +241,27 @@ sort_hist_kernel(int bits, int passes, const int64_t *__restrict__ indices, Tabl
                 atomicAdd(&h[p][(key[i] >> shift) & ((1u << nb) - 1u)], 1u);
                 shift += nb;
             }
+            if (msd_shift >= 0)
+                atomicAdd(&h[passes][(key[i] >> msd_shift) & (kRadix - 1u)], 1u);
         }
     }
     if (oob)
         raise_flag(err, DLRM_FLAG_INDEX_OOB);
     __syncthreads();
-    uint32_t *row = w.tile_hist + ((size_t)blockIdx.x * kMaxPasses) * kRadix;
-    for (int i = tid; i < passes * kRadix; i += kThreads)
+    uint32_t *row = w.tile_hist + ((size_t)blockIdx.x * kSortRows) * kRadix;
+    const int rows = passes + (msd_shift >= 0 ? 1 : 0);
+    for (int i = tid; i < rows * kRadix; i += kThreads)
         row[i] = (&h[0][0])[i];
 }
 
 // One CTA per (pass, table): sums the digit counts of the table's tiles
 // (four groups of kRadix threads, one thread per digit, each over every
 // fourth row) and scans them into the start position of each digit's keys in
-// the table's sorted range.
+// the table's sorted range.  For the MSD digit's row (`msd_row`) a bucket of
+// more than kTile keys sets kMsdOverflow before any pass runs.
 constexpr int kScanGroups = 4;
 __global__ void __launch_bounds__(kScanGroups * kRadix)
-sort_digit_scan_kernel(int passes, int T, BwdPtrs w)
+sort_digit_scan_kernel(int msd_row, int T, BwdPtrs w)
 {
     __shared__ uint32_t part[kScanGroups][kRadix];
     __shared__ uint32_t wsum[kRadix / 32];
@@ -260,7 +269,7 @@ sort_digit_scan_kernel(int passes, int T, BwdPtrs w)
     const int tid = threadIdx.x, dg = tid % kRadix, g = tid / kRadix, lane = tid & 31, warp = tid >> 5;
     const uint32_t h0 = w.tile_base[t], h1 = w.tile_base[t + 1];
     const uint32_t *col = w.tile_hist + (size_t)p * kRadix + dg;
-    constexpr size_t kRow = (size_t)kMaxPasses * kRadix;  // words per tile
+    constexpr size_t kRow = (size_t)kSortRows * kRadix;  // words per tile
     uint32_t c = 0;
     uint32_t hb = h0 + g;
     for (; hb + 3 * kScanGroups < h1; hb += 4 * kScanGroups) {
@@ -278,6 +287,8 @@ sort_digit_scan_kernel(int passes, int T, BwdPtrs w)
 #pragma unroll
     for (int gi = 0; gi < kScanGroups; gi++)
         c += part[gi][dg];
+    if (p == msd_row && c > (uint32_t)kTile)
+        atomicExch(w.msd_state, kMsdOverflow);
     uint32_t incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -322,9 +333,18 @@ __device__ __forceinline__ uint64_t load_status(const uint64_t *p)
 // look-back), and scatters its keys, in stable order, to the digit ranges
 // found by the histogram kernel.  A wait that runs out raises
 // DLRM_FLAG_WAIT_TIMEOUT and writes stay inside the table's range.
+// The first pass (pass 0, which reads the indices) sorts by the top 8 row
+// bits when the MSD sort is planned and no bucket is too large (`msd_d`), by
+// the lowest digit otherwise (`lsd_d`); the later LSD passes leave at once
+// after an MSD pass.  A digit names its shift and width, the tile counter and
+// the row of digit counts it uses.
+struct PassDigit {
+    int shift, nbits, ctr, crow;
+};
+constexpr int kRoleFirst = 1, kRoleLsd = 0;
 __global__ void __launch_bounds__(kSortThreads, 4)
-sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__ indices, TableSet ts, int T,
-                     BwdPtrs w, int spin_limit, int32_t *err)
+sort_onesweep_kernel(int pass, PassDigit lsd_d, PassDigit msd_d, int role, const int64_t *__restrict__ indices,
+                     TableSet ts, int T, BwdPtrs w, int spin_limit, int32_t *err)
 {
     __shared__ uint32_t skey[kTile];
     __shared__ uint32_t sval[kTile];
@@ -336,11 +356,16 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
     __shared__ TileInfo ti;
     __shared__ uint32_t tau_s;
     __shared__ int timed_out;
+    const bool msd = *w.msd_state == kMsdPlanned;
+    if (role == kRoleLsd && msd)
+        return;
+    const PassDigit pd = role == kRoleFirst && msd ? msd_d : lsd_d;
+    const int shift = pd.shift, nbits = pd.nbits, ctr = pd.ctr, crow = pd.crow;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid < 32) {
         uint32_t tau = 0;
         if (lane == 0)
-            tau = atomicAdd(&w.tile_ctr[pass], 1u);
+            tau = atomicAdd(&w.tile_ctr[ctr], 1u);
         tau = __shfl_sync(0xffffffffu, tau, 0);
         find_tile_warp(tau, T, w.tile_base, w.tstart, ti);
         if (lane == 0) {
@@ -495,7 +520,7 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
             }
             store_status(stat + (size_t)tau * kRadix + tid, kInclusive, excl + total);
         }
-        gbase[tid] = w.counts[((size_t)pass * T + ti.t) * kRadix + tid] + excl;
+        gbase[tid] = w.counts[((size_t)crow * T + ti.t) * kRadix + tid] + excl;
     }
     __syncthreads();
     if (tid == 0 && timed_out) {
@@ -511,6 +536,159 @@ sort_onesweep_kernel(int pass, int shift, int nbits, const int64_t *__restrict__
         if (dest - tbeg < tlen) {
             keys_out[dest] = k;
             vals_out[dest] = sval[j];
+        }
+    }
+}
+
+// ------------------------------------------------------- bucket sort ---
+
+// After the pass on the top 8 row bits a table's keys lie in 256 buckets, each
+// in position order.  One CTA per (table, bucket) sorts the bucket's keys by
+// the remaining `lbits` low bits in shared memory, stably (LSD passes of at
+// most 9 bits: ranks within each warp's run of positions from ballots over the
+// digit bits, then a scan over digits and warps), and writes them to the
+// buffer the LSD passes would have ended in: the result is the full stable
+// sort.  The digit scan has checked that no bucket holds more than kTile keys
+// (else the first pass sorted by the lowest digit and this kernel does
+// nothing); a bucket's size is its count from that scan, so a larger one
+// means counts that disagree with the keys: the sort is then marked failed
+// (nothing is updated) and DLRM_FLAG_BAD_OFFSETS raised.
+constexpr int kBucketThreads = 256;  // 8 warps, at most 16 keys per thread
+constexpr int kBucketBits = 9;       // widest digit of the local passes
+constexpr int kBucketRadix = 1 << kBucketBits;
+__global__ void __launch_bounds__(kBucketThreads, 4)
+bucket_sort_kernel(int lbits, int lpasses, int crow, int out_buf, int T, BwdPtrs w, int32_t *err)
+{
+    __shared__ uint32_t skey[kTile];
+    __shared__ uint32_t sval[kTile];
+    __shared__ uint16_t whist[8][kBucketRadix];  // per warp and digit: count, then exclusive prefix (<= kTile)
+    __shared__ uint32_t tdig[kBucketRadix];
+    __shared__ uint32_t wsum[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the MSD pass gave up a wait (its order is invalid, and so the result), or did not run
+    if (*w.sort_failed || *w.msd_state != kMsdPlanned)
+        return;
+    const int t = blockIdx.x / kRadix, v = blockIdx.x % kRadix;
+    const uint32_t *cnt = w.counts + ((size_t)crow * T + t) * kRadix;
+    const uint32_t s = cnt[v], e = v + 1 < kRadix ? cnt[v + 1] : w.tstart[t + 1];
+    const uint32_t n = e - s;
+    if (n == 0)
+        return;
+    if (n > (uint32_t)kTile) {
+        if (tid == 0) {
+            atomicOr(w.sort_failed, 1u);
+            raise_flag(err, DLRM_FLAG_BAD_OFFSETS);
+        }
+        return;
+    }
+    // warp `warp` holds positions warp*span .. +span, item i at warp*span + 32 i + lane
+    const int nit = (int)((n + 8 * 32 - 1) / (8 * 32));  // items per thread, 1 .. 16
+    const uint32_t wb = (uint32_t)warp * (uint32_t)nit * 32u;
+    const uint32_t *kin = w.keys[0] + s, *vin = w.vals[0] + s;
+    uint32_t key[kItems], val[kItems];
+#pragma unroll
+    for (int i = 0; i < kItems; i++) {
+        const uint32_t j = wb + i * 32 + lane;
+        key[i] = 0u;
+        val[i] = 0u;
+        if (i < nit && j < n) {
+            key[i] = kin[j];
+            val[i] = vin[j];
+        }
+    }
+    int shift = 0;
+    for (int p = 0; p < lpasses; p++) {
+        const int nb = pass_bits(lbits, lpasses, p);
+        const uint32_t mask = (1u << nb) - 1u;
+        const int radix = 1 << nb;
+        for (int i = tid; i < 8 * kBucketRadix / 2; i += kBucketThreads)
+            reinterpret_cast<uint32_t *>(&whist[0][0])[i] = 0u;
+        __syncthreads();
+        uint32_t rank[kItems];
+#pragma unroll
+        for (int i = 0; i < kItems; i++) {
+            rank[i] = 0u;
+            if (i < nit) {  // uniform over the block
+                const bool valid = wb + i * 32 + lane < n;
+                const uint32_t digit = valid ? (key[i] >> shift) & mask : 0xffffffffu;
+                unsigned peers = __ballot_sync(0xffffffffu, valid);
+                if (!valid)
+                    peers = ~peers;
+                for (int b = 0; b < nb; b++) {
+                    const bool bit = (digit >> b) & 1u;
+                    const unsigned m = __ballot_sync(0xffffffffu, bit);
+                    peers &= bit ? m : ~m;
+                }
+                if (valid)
+                    rank[i] = whist[warp][digit] + __popc(peers & ((1u << lane) - 1u));
+                __syncwarp();
+                if (valid && lane == __ffs(peers) - 1)
+                    whist[warp][digit] = (uint16_t)(whist[warp][digit] + __popc(peers));
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        // digits 2 tid and 2 tid + 1: exclusive prefix over the warps and the
+        // digits' totals; then the exclusive scan of the totals over the digits
+        uint32_t tot[2] = {0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            const int dg = 2 * tid + k;
+            if (dg < radix) {
+                for (int wi = 0; wi < 8; wi++) {
+                    const uint32_t c = whist[wi][dg];
+                    whist[wi][dg] = (uint16_t)tot[k];
+                    tot[k] += c;
+                }
+            }
+        }
+        const uint32_t mine = tot[0] + tot[1];
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += x;
+        }
+        if (lane == 31)
+            wsum[warp] = incl;
+        __syncthreads();
+        uint32_t before = incl - mine;
+        for (int wi = 0; wi < warp; wi++)
+            before += wsum[wi];
+        if (2 * tid < radix)
+            tdig[2 * tid] = before;
+        if (2 * tid + 1 < radix)
+            tdig[2 * tid + 1] = before + tot[0];
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kItems; i++) {
+            if (i < nit && wb + i * 32 + lane < n) {
+                const uint32_t digit = (key[i] >> shift) & mask;
+                const uint32_t dest = tdig[digit] + whist[warp][digit] + rank[i];
+                skey[dest] = key[i];
+                sval[dest] = val[i];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kItems; i++) {
+            const uint32_t j = wb + i * 32 + lane;
+            if (i < nit && j < n) {
+                key[i] = skey[j];
+                val[i] = sval[j];
+            }
+        }
+        __syncthreads();  // before the next pass clears the counts and overwrites the keys
+        shift += nb;
+    }
+    uint32_t *kout = w.keys[out_buf] + s, *vout = w.vals[out_buf] + s;
+#pragma unroll
+    for (int i = 0; i < kItems; i++) {
+        const uint32_t j = wb + i * 32 + lane;
+        if (i < nit && j < n) {
+            kout[j] = key[i];
+            vout[j] = val[i];
         }
     }
 }
@@ -628,11 +806,11 @@ seg_scan_kernel(int T, int64_t nnz, BwdPtrs w)
 
 // ---------------------------------------------------------------- host ---
 
-static int row_bits(const TableSet &ts, int T)
+static int row_bits(const int64_t *rows, int T)
 {
     int64_t maxr = 1;
     for (int t = 0; t < T; t++)
-        maxr = ts.rows[t] > maxr ? ts.rows[t] : maxr;
+        maxr = rows[t] > maxr ? rows[t] : maxr;
     int bits = 1;
     while (bits < 32 && ((int64_t)1 << bits) < maxr)
         bits++;
@@ -672,9 +850,10 @@ static BwdPtrs bind_workspace(int T, int64_t nnz, int d, void *workspace)
     w.status[0] = reinterpret_cast<uint64_t *>(base + L.status[0]);
     w.status[1] = reinterpret_cast<uint64_t *>(base + L.status[1]);
     w.tile_ctr = reinterpret_cast<uint32_t *>(base + L.tile_ctr);
-    w.sort_failed = w.tile_ctr + kMaxPasses;
-    w.vals_bags = w.tile_ctr + kMaxPasses + 1;
-    w.ids_ready = w.tile_ctr + kMaxPasses + 2;
+    w.sort_failed = w.tile_ctr + kMaxPasses + 1;
+    w.vals_bags = w.tile_ctr + kMaxPasses + 2;
+    w.ids_ready = w.tile_ctr + kMaxPasses + 3;
+    w.msd_state = w.tile_ctr + kMaxPasses + 4;
     w.tile_hist = reinterpret_cast<uint32_t *>(base + L.tile_hist);
     w.counts = reinterpret_cast<uint32_t *>(base + L.counts);
     w.tstart = reinterpret_cast<uint32_t *>(base + L.tstart);
@@ -699,9 +878,35 @@ static BwdPtrs bind_workspace(int T, int64_t nnz, int d, void *workspace)
 // holding the sorted keys (both halves of the backward derive them alike).
 static void sort_plan(const TableSet &ts, int T, int &bits, int &passes, int &final_buf)
 {
-    bits = row_bits(ts, T);
+    bits = row_bits(ts.rows, T);
     passes = (bits + kRadixBits - 1) / kRadixBits;
     final_buf = (passes - 1) & 1;
+}
+
+// Whether the coalescing sorts by the top 8 row bits first and then each
+// bucket in shared memory, one pass over all keys instead of three or four:
+// for rows of 17 bits or more, every table above half the largest power of
+// two (so that its keys spread over the buckets) and buckets of 256 to 2560
+// keys on average (the shape of uniform lookups into large tables).  Lookups
+// skewed enough that a bucket outgrows a tile fall back to the LSD passes on
+// the device.
+constexpr int64_t kMsdMinAvg = 256, kMsdMaxAvg = 2560;
+static bool use_msd(const int64_t *rows, int bits, int T, int64_t nnz)
+{
+    const int64_t buckets = (int64_t)T * kRadix;
+    if (bits < 17 || nnz < buckets * kMsdMinAvg || nnz > buckets * kMsdMaxAvg)
+        return false;
+    for (int t = 0; t < T; t++)
+        if (rows[t] <= ((int64_t)1 << (bits - 1)))
+            return false;
+    return true;
+}
+
+void coalesce_plan(const int64_t *rows, int T, int64_t nnz, int &passes, bool &msd)
+{
+    const int bits = row_bits(rows, T);
+    passes = (bits + kRadixBits - 1) / kRadixBits;
+    msd = use_msd(rows, bits, T, nnz);
 }
 
 // Numbers the unique keys of a coalescing (their runs' starts counted per
@@ -741,7 +946,9 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
     // without a view the sort carries each lookup's bag (read in position order in the first pass),
     // so the reduce need not gather it by position; the view keeps the positions
     const uint32_t vals_bags = view ? 0u : 1u;
-    bwd_prep_kernel<<<1, 256, 0, st>>>(offsets, T, B, nnz, w, hooks.sort_first_tile, vals_bags, err);
+    const bool msd = use_msd(ts.rows, bits, T, nnz);
+    bwd_prep_kernel<<<1, 256, 0, st>>>(offsets, T, B, nnz, w, hooks.sort_first_tile, vals_bags, msd ? 1u : 0u,
+                                       err);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
@@ -759,22 +966,36 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
             return s;
     }
     const int64_t grid = L.ntiles_max;
-    sort_hist_kernel<<<(unsigned)grid, 2 * kSortThreads, 0, st>>>(bits, passes, indices, ts, T, w, err);
+    const int lbits = bits - kRadixBits;  // below the MSD digit
+    sort_hist_kernel<<<(unsigned)grid, 2 * kSortThreads, 0, st>>>(bits, passes, msd ? lbits : -1, indices, ts, T,
+                                                                   w, err);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
-    sort_digit_scan_kernel<<<(unsigned)(passes * T), kScanGroups * kRadix, 0, st>>>(passes, T, w);
+    const int rows = passes + (msd ? 1 : 0);  // the MSD digit's counts are row `passes`
+    sort_digit_scan_kernel<<<(unsigned)(rows * T), kScanGroups * kRadix, 0, st>>>(msd ? passes : -1, T, w);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
+    // with the MSD sort: the first launch sorts by the top digit (unless the digit scan found a
+    // bucket too large), the bucket sort follows, and the later LSD passes leave at once
+    const PassDigit msd_d{lbits, kRadixBits, kMaxPasses, passes};
     int shift = 0;
     for (int p = 0; p < passes; p++) {
         const int nb = pass_bits(bits, passes, p);
-        sort_onesweep_kernel<<<(unsigned)grid, kSortThreads, 0, st>>>(p, shift, nb, indices, ts, T, w,
-                                                                      hooks.sort_polls, err);
+        const PassDigit lsd_d{shift, nb, p, p};
+        sort_onesweep_kernel<<<(unsigned)grid, kSortThreads, 0, st>>>(p, lsd_d, msd_d, p == 0 ? kRoleFirst : kRoleLsd,
+                                                                      indices, ts, T, w, hooks.sort_polls, err);
         count_launch(st);
         if ((s = launch_status()) != DLRM_OK)
             return s;
+        if (p == 0 && msd) {
+            bucket_sort_kernel<<<(unsigned)(T * kRadix), kBucketThreads, 0, st>>>(
+                lbits, (lbits + kBucketBits - 1) / kBucketBits, passes, final_buf, T, w, err);
+            count_launch(st);
+            if ((s = launch_status()) != DLRM_OK)
+                return s;
+        }
         shift += nb;
     }
     if (!view)  // the unique keys are numbered for a view, or by the reduce for gradient rows

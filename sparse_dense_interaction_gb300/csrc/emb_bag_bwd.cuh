@@ -11,7 +11,10 @@ constexpr int kSortThreads = 256;             // 8 warps
 constexpr int kItems = kTile / kSortThreads;  // 16 per thread
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
-constexpr int kMaxPasses = 4;
+constexpr int kMaxPasses = 4;                 // LSD passes of up to 8 bits over 32-bit rows
+constexpr int kSortRows = kMaxPasses + 1;     // digit-count rows: the LSD passes' and the MSD digit's
+constexpr uint32_t kMsdPlanned = 1u;          // sorted by the top 8 row bits, then per bucket
+constexpr uint32_t kMsdOverflow = 2u;         // a bucket exceeded a tile: the LSD passes sort instead
 constexpr uint32_t kSentinel = 0xffffffffu;   // sort key of an out-of-range index
 constexpr uint32_t kHasHead = 1u, kHeadEnds = 2u, kHasTail = 4u;
 constexpr int kReduceThreads = 256;           // 8 warps per tile in the reduce, one or two chunks each
@@ -27,6 +30,7 @@ struct BwdPtrs {
     uint32_t *sort_failed;  // set by a radix pass whose wait ran out: the reduce then updates nothing
     uint32_t *vals_bags;    // 1: the sort carried each lookup's bag (no view asked for); 0: its position
     uint32_t *ids_ready;    // 1: the unique keys are numbered (tile_ubase, num_unique): a view or gradient rows
+    uint32_t *msd_state;    // kMsdPlanned: sorted by the top digit and per bucket; kMsdOverflow: LSD passes
     uint32_t *chunk_tail_row;  // row and table of the run that leaves each chunk (read by the finalize)
     int32_t *chunk_tail_t;
     int32_t *uniq_table;

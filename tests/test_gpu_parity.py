@@ -290,7 +290,14 @@ BWD_CASES = {
     "d512-f32": dict(name="tiny", B=300, rows=[300, 20], d=512, bag=("poisson", 5.0, 0, 12)),
     # 40 tables: the sort's tiles find their table by a search, not by one warp's ballot
     "40-tables": dict(name="multi-hot", B=200, T=40, rows=[3000] * 40),
+    # rows of 18-19 bits and 256-2560 keys per top-digit bucket: one pass on the top 8 bits and a
+    # shared-memory sort per bucket; with Zipf indices a hot row overflows its bucket and the LSD
+    # passes sort on the device instead
+    "msd-f32": dict(name="capacity", B=4096, rows=[200000, 150001]),
+    "msd-f16-poisson": dict(name="multi-hot", B=6000, T=3, rows=[300000, 270000, 524288], index=("uniform",)),
+    "msd-overflow-zipf": dict(name="capacity", B=4096, rows=[200000, 150001], index=("zipf", 1.2)),
 }
+MSD_CASES = ("msd-f32", "msd-f16-poisson", "msd-overflow-zipf")
 
 
 def _run_bwd(cfg, host, offsets, indices, dp, lr, grad_cap=None, want_view=True):
@@ -324,6 +331,16 @@ def test_emb_bag_bwd_sgd_without_a_view_gives_the_same_bits(case):
     np.testing.assert_array_equal(g_bags.cpu().numpy().view(np.uint32), g_view.cpu().numpy().view(np.uint32))
     for t in range(cfg["T"]):
         np.testing.assert_array_equal(device_table_bits(t_bags[t]), device_table_bits(t_view[t]))
+
+
+def test_msd_cases_take_the_bucket_sort():
+    for case in MSD_CASES:
+        c = dict(BWD_CASES[case])
+        cfg = W.make_config(c.pop("name"), **c)
+        nnz = W.make_indices(cfg)[1].size
+        assert sdi.dlrm_emb_bag_sort_plan(cfg["rows"], nnz)[1], case
+    cfg = W.make_config("multi-hot", B=6000, T=3, rows=[300000, 1000, 524288])  # a small table: LSD
+    assert not sdi.dlrm_emb_bag_sort_plan(cfg["rows"], W.make_indices(cfg)[1].size)[1]
 
 
 def _check_coalesce(view, co, nnz):
