@@ -455,6 +455,35 @@ class KernelProfiler:
         return out
 
 
+class CallTimer:
+    """Brackets every library call (not each of its kernels) with CUDA events:
+    a call's time without the events the per-kernel profile inserts between
+    its kernels."""
+
+    def __init__(self, torch, stream, n_steps):
+        self.torch, self.stream = torch, stream
+        self.pool = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(n_steps * 5)]
+        self.next, self.calls, self.cur = 0, [], None
+
+    def begin(self, name, stream=None):
+        a, b = self.pool[self.next]
+        self.next += 1
+        a.record(stream if stream is not None else self.stream)
+        self.cur = (name, a, b, stream if stream is not None else self.stream)
+
+    def end(self):
+        name, a, b, stream = self.cur
+        b.record(stream)
+        self.calls.append((name, a, b))
+
+    def per_call_ms(self):
+        out = {}
+        for name, a, b in self.calls:
+            out.setdefault(name, []).append(a.elapsed_time(b))
+        return {k: float(np.mean(v)) for k, v in out.items()}
+
+
 BWD_KERNELS_PREFIX = ["bwd_prep", "bag_ids"]
 
 
@@ -545,9 +574,11 @@ def stage_times(kernel_ms, plan):
 
 
 def measure_target(name, args, dev, update="sorted"):
-    """One workload measured stage by stage (serial schedule, kernel events):
-    the lookup, the coalescing, the reduce and the whole backward, each with
-    its algorithmic bytes and its fraction of the measured HBM peak."""
+    """One workload measured stage by stage (serial schedule): the lookup and
+    the whole backward timed per call (CUDA events around each library call),
+    the coalescing and the reduce from a second run with every kernel
+    bracketed by events; each with its algorithmic bytes and its fraction of
+    the measured HBM peak."""
     import torch
 
     import sparse_dense_interaction_gb300 as sdi
@@ -560,21 +591,30 @@ def measure_target(name, args, dev, update="sorted"):
     if sdi.dlrm_read_error(st.flag) != 0:
         raise RuntimeError(f"device error flag in the {name} target")
     K = args.target_steps
-    prof = KernelProfiler(torch, sdi, stream, K)
+    calls = CallTimer(torch, stream, K)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(K):
-        st.run(prof)
+        st.run(calls)
     b.record(stream)
     torch.cuda.synchronize()
     ms_step = a.elapsed_time(b) / K
+    call_ms = calls.per_call_ms()
+    prof = KernelProfiler(torch, sdi, stream, K)
+    for _ in range(K):
+        st.run(prof)
+    torch.cuda.synchronize()
     plan = sdi.dlrm_emb_bag_sort_plan(cfg["rows"], st.nnz)
     kernel_ms = {kernel_name(c, k, plan, st.grad is not None): float(np.mean(v))
                  for (c, k), v in prof.per_kernel_ms().items()}
     alg, uniq = algorithmic_bytes(cfg, st)
     peak, _ = measured_peaks()
     stages = {}
-    for stage, ms in stage_times(kernel_ms, plan).items():
+    times = stage_times(kernel_ms, plan)
+    kernel_sum_bwd = times.get("backward")
+    times["lookup"] = call_ms.get("emb_bag_fwd")  # one kernel: call and kernel times agree
+    times["backward"] = call_ms.get("emb_bag_bwd_atomic" if update == "atomic" else "emb_bag_bwd")
+    for stage, ms in times.items():
         if ms is None:
             continue
         nbytes = {"lookup": alg["emb_bag_fwd"], "reduce": alg["seg_reduce"], "backward": alg["backward"]}.get(stage)
@@ -590,10 +630,13 @@ def measure_target(name, args, dev, update="sorted"):
         for stage, kern in (("reduce", "seg_reduce"), ("backward", "emb_bag_bwd_atomic")):
             if stage in stages and kern in tr and (stage == "reduce" or update == "atomic"):
                 stages[stage]["traffic"] = tr[kern]
+    if "backward" in stages and kernel_sum_bwd is not None:
+        stages["backward"]["kernel_sum_ms"] = kernel_sum_bwd  # with events between its kernels
     out = {"config": config_of(cfg), "update": update, "ms_per_step": ms_step,
            "samples_per_s": cfg["B"] / (ms_step / 1e3), "steps": K, "unique_rows": uniq, "lookups": st.nnz,
-           "stages": stages}
-    del st, prof
+           "stages": stages, "stage_timing": "lookup and backward: events around each library call; coalescing "
+                                             "and reduce: sums of per-kernel events (a second run)"}
+    del st, prof, calls
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return out
