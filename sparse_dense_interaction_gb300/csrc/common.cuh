@@ -138,32 +138,4 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { retu
 __device__ __forceinline__ int64_t load_stream(const int64_t *p) { return __ldcs(p); }
 __device__ __forceinline__ uint4 load_table(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 
-// Kernels of one call launched back to back with programmatic stream
-// serialization: a kernel's CTAs may be scheduled while the kernel before it
-// on the stream runs its last CTAs.  Each kernel launched this way calls
-// chain_entry() first: it waits until the kernel before it has completed and
-// its writes are visible (so the stream order holds for every kernel before
-// it), then lets the next kernel be scheduled.
-__device__ __forceinline__ void chain_entry()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-template <typename... P, typename... A>
-inline cudaError_t launch_chained(void (*kernel)(P...), unsigned grid, unsigned block, cudaStream_t st, A... args)
-{
-    cudaLaunchConfig_t c = {};
-    c.gridDim = dim3(grid);
-    c.blockDim = dim3(block);
-    c.dynamicSmemBytes = 0;
-    c.stream = st;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    c.attrs = at;
-    c.numAttrs = 1;
-    return cudaLaunchKernelEx(&c, kernel, args...);
-}
-
 }  // namespace dlrm

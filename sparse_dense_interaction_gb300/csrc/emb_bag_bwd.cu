@@ -87,7 +87,6 @@ __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nnz, BwdPtrs w,
                 uint32_t first_tile, uint32_t vals_bags, uint32_t msd, int32_t *err)
 {
-    chain_entry();
     __shared__ int64_t start[DLRM_MAX_TABLES + 1];
     for (int t = threadIdx.x; t <= T; t += blockDim.x)
         start[t] = offsets[(int64_t)t * B];
@@ -139,7 +138,6 @@ __global__ void __launch_bounds__(256)
 bag_ids_kernel(const int64_t *__restrict__ offsets, int T, int64_t B, int64_t nnz,
                uint32_t *__restrict__ bag_of, int32_t *err)
 {
-    chain_entry();
     const int lane = threadIdx.x & 31;
     const int64_t nbags = (int64_t)T * B;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -210,7 +208,6 @@ __global__ void __launch_bounds__(2 * kSortThreads)
 sort_hist_kernel(int bits, int passes, int msd_shift, const int64_t *__restrict__ indices, TableSet ts, int T,
                  BwdPtrs w, int32_t *err)
 {
-    chain_entry();
     constexpr int kThreads = 2 * kSortThreads;  // 512: one CTA per tile, 8 indices per thread in flight
     __shared__ uint32_t h[kSortRows][kRadix];
     __shared__ TileInfo ti;
@@ -266,7 +263,6 @@ constexpr int kScanGroups = 4;
 __global__ void __launch_bounds__(kScanGroups * kRadix)
 sort_digit_scan_kernel(int msd_row, int T, BwdPtrs w)
 {
-    chain_entry();
     __shared__ uint32_t part[kScanGroups][kRadix];
     __shared__ uint32_t wsum[kRadix / 32];
     const int p = blockIdx.x / T, t = blockIdx.x % T;
@@ -350,7 +346,6 @@ __global__ void __launch_bounds__(kSortThreads, 4)
 sort_onesweep_kernel(int pass, PassDigit lsd_d, PassDigit msd_d, int role, const int64_t *__restrict__ indices,
                      TableSet ts, int T, BwdPtrs w, int spin_limit, int32_t *err)
 {
-    chain_entry();
     __shared__ uint32_t skey[kTile];
     __shared__ uint32_t sval[kTile];
     __shared__ uint32_t whist[8][kRadix];
@@ -564,7 +559,6 @@ constexpr int kBucketRadix = 1 << kBucketBits;
 __global__ void __launch_bounds__(kBucketThreads, 4)
 bucket_sort_kernel(int lbits, int lpasses, int crow, int out_buf, int T, BwdPtrs w, int32_t *err)
 {
-    chain_entry();
     __shared__ uint32_t skey[kTile];
     __shared__ uint32_t sval[kTile];
     __shared__ uint16_t whist[8][kBucketRadix];  // per warp and digit: count, then exclusive prefix (<= kTile)
@@ -709,7 +703,6 @@ bucket_sort_kernel(int lbits, int lpasses, int crow, int out_buf, int T, BwdPtrs
 __global__ void __launch_bounds__(256)
 seg_count_kernel(int T, int final_buf, BwdPtrs w)
 {
-    chain_entry();
     __shared__ TileInfo ti;
     __shared__ uint32_t wc[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -756,7 +749,6 @@ seg_count_kernel(int T, int final_buf, BwdPtrs w)
 __global__ void __launch_bounds__(1024)
 seg_scan_kernel(int T, int64_t nnz, BwdPtrs w)
 {
-    chain_entry();
     __shared__ uint32_t wsum[32];
     __shared__ uint32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -925,12 +917,12 @@ void coalesce_plan(const int64_t *rows, int T, int64_t nnz, int &passes, bool &m
 // these numbers; the update itself does not need them.
 static int launch_number_keys(int T, int64_t nnz, int final_buf, int64_t grid, BwdPtrs w, cudaStream_t st)
 {
-    launch_chained(seg_count_kernel, (unsigned)grid, 256, st, T, final_buf, w);
+    seg_count_kernel<<<(unsigned)grid, 256, 0, st>>>(T, final_buf, w);
     count_launch(st);
     int s = launch_status();
     if (s != DLRM_OK)
         return s;
-    launch_chained(seg_scan_kernel, 1, 1024, st, T, nnz, w);
+    seg_scan_kernel<<<1, 1024, 0, st>>>(T, nnz, w);
     count_launch(st);
     return launch_status();
 }
@@ -958,8 +950,8 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
     // so the reduce need not gather it by position; the view keeps the positions
     const uint32_t vals_bags = view ? 0u : 1u;
     const bool msd = use_msd(ts.rows, bits, T, nnz);
-    launch_chained(bwd_prep_kernel, 1, 256, st, offsets, T, B, nnz, w, hooks.sort_first_tile, vals_bags,
-                   msd ? 1u : 0u, err);
+    bwd_prep_kernel<<<1, 256, 0, st>>>(offsets, T, B, nnz, w, hooks.sort_first_tile, vals_bags, msd ? 1u : 0u,
+                                       err);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
@@ -971,20 +963,20 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
         const int64_t nbags = (int64_t)T * B;
         int64_t grid = (nbags + 255) / 256;  // 8 warps of 32 bags per block
         const int64_t cap = (int64_t)sm_count() * 8;
-        launch_chained(bag_ids_kernel, (unsigned)(grid < cap ? grid : cap), 256, st, offsets, T, B, nnz, w.bag_of, err);
+        bag_ids_kernel<<<(unsigned)(grid < cap ? grid : cap), 256, 0, st>>>(offsets, T, B, nnz, w.bag_of, err);
         count_launch(st);
         if ((s = launch_status()) != DLRM_OK)
             return s;
     }
     const int64_t grid = L.ntiles_max;
     const int lbits = bits - kRadixBits;  // below the MSD digit
-    launch_chained(sort_hist_kernel, (unsigned)grid, 2 * kSortThreads, st, bits, passes, msd ? lbits : -1, indices, ts,
-                   T, w, err);
+    sort_hist_kernel<<<(unsigned)grid, 2 * kSortThreads, 0, st>>>(bits, passes, msd ? lbits : -1, indices, ts, T,
+                                                                   w, err);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
     const int rows = passes + (msd ? 1 : 0);  // the MSD digit's counts are row `passes`
-    launch_chained(sort_digit_scan_kernel, (unsigned)(rows * T), kScanGroups * kRadix, st, msd ? passes : -1, T, w);
+    sort_digit_scan_kernel<<<(unsigned)(rows * T), kScanGroups * kRadix, 0, st>>>(msd ? passes : -1, T, w);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
@@ -995,14 +987,14 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
     for (int p = 0; p < passes; p++) {
         const int nb = pass_bits(bits, passes, p);
         const PassDigit lsd_d{shift, nb, p, p};
-        launch_chained(sort_onesweep_kernel, (unsigned)grid, kSortThreads, st, p, lsd_d, msd_d,
-                       p == 0 ? kRoleFirst : kRoleLsd, indices, ts, T, w, hooks.sort_polls, err);
+        sort_onesweep_kernel<<<(unsigned)grid, kSortThreads, 0, st>>>(p, lsd_d, msd_d, p == 0 ? kRoleFirst : kRoleLsd,
+                                                                      indices, ts, T, w, hooks.sort_polls, err);
         count_launch(st);
         if ((s = launch_status()) != DLRM_OK)
             return s;
         if (p == 0 && msd) {
-            launch_chained(bucket_sort_kernel, (unsigned)(T * kRadix), kBucketThreads, st, lbits,
-                           (lbits + kBucketBits - 1) / kBucketBits, passes, final_buf, T, w, err);
+            bucket_sort_kernel<<<(unsigned)(T * kRadix), kBucketThreads, 0, st>>>(
+                lbits, (lbits + kBucketBits - 1) / kBucketBits, passes, final_buf, T, w, err);
             count_launch(st);
             if ((s = launch_status()) != DLRM_OK)
                 return s;

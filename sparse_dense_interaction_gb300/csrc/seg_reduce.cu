@@ -152,7 +152,6 @@ template <typename TT, int VEC, int G, int C, int U, int PD, bool FULL>
 __global__ void __launch_bounds__(kReduceThreads, 4)
 seg_reduce_kernel(ReduceArgs a, BwdPtrs w)
 {
-    chain_entry();
     using V = Vec<VEC>;
     using F = typename V::F;
     using RC = RowChunk<TT, VEC>;
@@ -467,7 +466,6 @@ template <int VEC>
 __global__ void __launch_bounds__(256)
 seg_block_sum_kernel(ReduceArgs a, BwdPtrs w, int NS)
 {
-    chain_entry();
     if (*w.sort_failed)
         return;
     using V = Vec<VEC>;
@@ -503,7 +501,6 @@ template <typename TT, int VEC, int NB>
 __global__ void __launch_bounds__(256)
 seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
 {
-    chain_entry();
     if (*w.sort_failed)
         return;
     using V = Vec<VEC>;
@@ -616,8 +613,6 @@ seg_finalize_kernel(ReduceArgs a, BwdPtrs w, int NS)
 template <typename TT, int VEC, int G, int C, int U, int PD>
 static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaStream_t st)
 {
-    // an ordinary launch: scheduled ahead, while the coalescing's last kernel finishes, the
-    // reduce's CTAs made uniform multi-hot's backward 5 % slower (its small kernels are chained)
     if (a.d % (G * C * VEC) == 0)
         seg_reduce_kernel<TT, VEC, G, C, U, PD, true><<<(unsigned)grid, kReduceThreads, 0, st>>>(a, w);
     else
@@ -629,12 +624,12 @@ static int run_reduce(const ReduceArgs &a, const BwdPtrs &w, int64_t grid, cudaS
     constexpr int NS = (kReduceThreads / 32) * (32 / G);
     const int64_t chunks = grid * NS;
     const int64_t blocks = (chunks + kFinalizeBlock - 1) / kFinalizeBlock;  // one warp per block of chunks
-    launch_chained(seg_block_sum_kernel<VEC>, (unsigned)((blocks + 7) / 8), 256, st, a, w, NS);
+    seg_block_sum_kernel<VEC><<<(unsigned)((blocks + 7) / 8), 256, 0, st>>>(a, w, NS);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;
     // AdaGrad holds whole rows: 2 x 128 (vectorised) or 8 x 32 (scalar) elements
-    launch_chained(seg_finalize_kernel<TT, VEC, kAdagradMaxD / (32 * VEC)>, (unsigned)((chunks + 7) / 8), 256, st, a, w, NS);
+    seg_finalize_kernel<TT, VEC, kAdagradMaxD / (32 * VEC)><<<(unsigned)((chunks + 7) / 8), 256, 0, st>>>(a, w, NS);
     count_launch(st);
     return launch_status();
 }
