@@ -56,13 +56,25 @@ def _guards_intact(buf, nbytes):
     return bool((b[:GUARD] == 0xA5).all() and (b[GUARD + nbytes:] == 0xA5).all())
 
 
-def test_sort_lookback_wait_runs_out_and_nothing_is_updated():
-    # one table with four sort tiles; the passes start claiming at tile 1, so
-    # tile 1 waits for tile 0's digit counts, which never come
-    cfg = W.make_config("capacity", T=1, rows=[50000], B=400, bag=("fixed", 32))
+SORT_WAIT_CASES = {
+    # one table with four sort tiles, sorted by LSD passes
+    "lsd": (dict(T=1, rows=[50000], B=400, bag=("fixed", 32)), False),
+    # 18-bit rows and 256 keys per top-digit bucket: the top-digit pass waits, and the bucket
+    # sort and the LSD passes after it must leave everything alone
+    "bucket": (dict(T=1, rows=[200000], B=2048, bag=("fixed", 32)), True),
+}
+
+
+@pytest.mark.parametrize("plan", sorted(SORT_WAIT_CASES))
+def test_sort_lookback_wait_runs_out_and_nothing_is_updated(plan):
+    # the passes start claiming at tile 1, so tile 1 waits for tile 0's digit
+    # counts, which never come
+    over, msd = SORT_WAIT_CASES[plan]
+    cfg = W.make_config("capacity", **over)
     host = W.tables_host(cfg)
     offsets, indices = W.make_indices(cfg)
     assert indices.size > 3 * 4096
+    assert sdi.dlrm_emb_bag_sort_plan(cfg["rows"], indices.size)[1] == msd
     dp = W.make_dpooled(cfg)
     nbytes = sdi.dlrm_emb_bag_bwd_workspace_size(1, cfg["B"], indices.size, cfg["d"])
     buf, ws = _guarded_workspace(nbytes)
