@@ -16,7 +16,11 @@
 //                counts the digits of every pass per table; then one kernel
 //                per pass ranks each tile in shared memory (warp match +
 //                per-warp histograms), finds the counts of the tiles before
-//                it by decoupled look-back, and scatters coalesced.
+//                it by decoupled look-back, and scatters coalesced.  For
+//                uniform lookups into large tables the first pass sorts by
+//                the top 8 row bits instead and one CTA per bucket finishes
+//                the sort in shared memory, unless the digit counts show a
+//                bucket larger than a tile.
 //  4. count      run starts (a new row, or a table's first lookup) per tile
 //  5. scan       exclusive scan of the per-tile counts: the runs' unique ids
 //  6. reduce     per tile, the summed pooled gradient of every run of equal
