@@ -573,6 +573,37 @@ def stage_times(kernel_ms, plan):
     return out
 
 
+def measure_overlapped_step(name, args, dev):
+    """The step of a workload with the coalescing on a second stream beside the
+    lookup (the schedule a training loop would use): CUDA events around the
+    steps only."""
+    import torch
+
+    import sparse_dense_interaction_gb300 as sdi
+    cfg = W.make_config(name)
+    st = Step(cfg, args.seed, dev, "overlap", "separate", "sgd", "sorted")
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        st.run()
+    torch.cuda.synchronize()
+    if sdi.dlrm_read_error(st.flag) != 0:
+        raise RuntimeError(f"device error flag in the overlapped {name} step")
+    K = args.target_steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        st.run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_step = a.elapsed_time(b) / K
+    out = {"config": config_of(cfg), "update": "sorted", "schedule": "overlap", "ms_per_step": ms_step,
+           "samples_per_s": cfg["B"] / (ms_step / 1e3), "steps": K}
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_target(name, args, dev, update="sorted"):
     """One workload measured stage by stage (serial schedule): the lookup and
     the whole backward timed per call (CUDA events around each library call),
@@ -650,6 +681,7 @@ def run_targets(args, dev):
     for key, name, update in (("capacity", "capacity", "sorted"), ("capacity_atomic", "capacity", "atomic"),
                               ("multi_hot_uniform", "multi-hot-uniform", "sorted")):
         out[key] = measure_target(name, args, dev, update)
+    out["capacity_overlapped"] = measure_overlapped_step("capacity", args, dev)
     return out
 
 

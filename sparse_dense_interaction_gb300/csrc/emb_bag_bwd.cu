@@ -618,13 +618,10 @@ bucket_sort_kernel(int lbits, int lpasses, int crow, int out_buf, int T, BwdPtrs
                 unsigned peers = __ballot_sync(0xffffffffu, valid);
                 if (!valid)
                     peers = ~peers;
-#pragma unroll
-                for (int b = 0; b < kBucketBits; b++) {
-                    if (b < nb) {  // uniform over the block
-                        const bool bit = (digit >> b) & 1u;
-                        const unsigned m = __ballot_sync(0xffffffffu, bit);
-                        peers &= bit ? m : ~m;
-                    }
+                for (int b = 0; b < nb; b++) {  // a loop: unrolled and predicated it ran 35 % slower
+                    const bool bit = (digit >> b) & 1u;
+                    const unsigned m = __ballot_sync(0xffffffffu, bit);
+                    peers &= bit ? m : ~m;
                 }
                 if (valid)
                     rank[i] = whist[warp][digit] + __popc(peers & ((1u << lane) - 1u));
