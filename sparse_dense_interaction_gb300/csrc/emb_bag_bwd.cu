@@ -207,7 +207,7 @@ __host__ __device__ __forceinline__ int pass_bits(int bits, int passes, int p)
 // each pass finds the counts of the tiles before its own by looking back.
 // With msd_shift >= 0 row `passes` counts the top digit (key >> msd_shift)
 // for the pass that sorts by it first.  Also clears the look-back words of
-// pass 0 and flags indices out of range.
+// pass 1 (the first pass needs none) and flags indices out of range.
 __global__ void __launch_bounds__(2 * kSortThreads)
 sort_hist_kernel(int bits, int passes, int msd_shift, const int64_t *__restrict__ indices, TableSet ts, int T,
                  BwdPtrs w, int32_t *err)
@@ -225,7 +225,7 @@ sort_hist_kernel(int bits, int passes, int msd_shift, const int64_t *__restrict_
     if (!ti.valid)
         return;
     if (tid < kRadix)
-        w.status[0][(size_t)tau * kRadix + tid] = 0;
+        w.status[1][(size_t)tau * kRadix + tid] = 0;
     const int64_t R = ts.rows[ti.t];
     const uint32_t lo = ti.lo;
     uint32_t key[kTile / kThreads];
@@ -259,32 +259,73 @@ sort_hist_kernel(int bits, int passes, int msd_shift, const int64_t *__restrict_
 }
 
 // One CTA per (pass, table): sums the digit counts of the table's tiles
-// (four groups of kRadix threads, one thread per digit, each over every
-// fourth row) and scans them into the start position of each digit's keys in
-// the table's sorted range.  For the MSD digit's row (`msd_row`) a bucket of
-// more than kTile keys sets kMsdOverflow before any pass runs.
+// (four groups of kRadix threads, one thread per digit) and scans them into
+// the start position of each digit's keys in the table's sorted range.  For
+// the rows in `prefix_rows` (the first pass's: its tiles hold the keys in the
+// order the histogram counted them) the groups take consecutive quarters of
+// the tiles and replace each tile's counts by the exclusive prefix over the
+// table's earlier tiles, so the first pass finds its offsets without looking
+// back.  For the MSD digit's row (`msd_row`) a bucket of more than kTile keys
+// sets kMsdOverflow before any pass runs.
 constexpr int kScanGroups = 4;
 __global__ void __launch_bounds__(kScanGroups * kRadix)
-sort_digit_scan_kernel(int msd_row, int T, BwdPtrs w)
+sort_digit_scan_kernel(int msd_row, unsigned prefix_rows, int T, BwdPtrs w)
 {
     __shared__ uint32_t part[kScanGroups][kRadix];
     __shared__ uint32_t wsum[kRadix / 32];
     const int p = blockIdx.x / T, t = blockIdx.x % T;
     const int tid = threadIdx.x, dg = tid % kRadix, g = tid / kRadix, lane = tid & 31, warp = tid >> 5;
     const uint32_t h0 = w.tile_base[t], h1 = w.tile_base[t + 1];
-    const uint32_t *col = w.tile_hist + (size_t)p * kRadix + dg;
+    uint32_t *col = w.tile_hist + (size_t)p * kRadix + dg;
     constexpr size_t kRow = (size_t)kSortRows * kRadix;  // words per tile
-    uint32_t c = 0;
-    uint32_t hb = h0 + g;
-    for (; hb + 3 * kScanGroups < h1; hb += 4 * kScanGroups) {
-        const uint32_t a0 = col[hb * kRow], a1 = col[(hb + kScanGroups) * kRow];
-        const uint32_t a2 = col[(hb + 2 * kScanGroups) * kRow], a3 = col[(hb + 3 * kScanGroups) * kRow];
-        c += (a0 + a1) + (a2 + a3);
+    const bool prefix = (prefix_rows >> p) & 1u;
+    uint32_t c = 0, r0 = 0, r1 = 0;
+    if (prefix) {
+        const uint32_t n = h1 - h0, q = (n + kScanGroups - 1) / kScanGroups;
+        r0 = h0 + min((uint32_t)g * q, n);
+        r1 = h0 + min((uint32_t)(g + 1) * q, n);
+        uint32_t hb = r0;
+        for (; hb + 4 <= r1; hb += 4) {
+            const uint32_t a0 = col[hb * kRow], a1 = col[(hb + 1) * kRow];
+            const uint32_t a2 = col[(hb + 2) * kRow], a3 = col[(hb + 3) * kRow];
+            c += (a0 + a1) + (a2 + a3);
+        }
+        for (; hb < r1; hb++)
+            c += col[hb * kRow];
+    } else {
+        uint32_t hb = h0 + g;
+        for (; hb + 3 * kScanGroups < h1; hb += 4 * kScanGroups) {
+            const uint32_t a0 = col[hb * kRow], a1 = col[(hb + kScanGroups) * kRow];
+            const uint32_t a2 = col[(hb + 2 * kScanGroups) * kRow], a3 = col[(hb + 3 * kScanGroups) * kRow];
+            c += (a0 + a1) + (a2 + a3);
+        }
+        for (; hb < h1; hb += kScanGroups)
+            c += col[hb * kRow];
     }
-    for (; hb < h1; hb += kScanGroups)
-        c += col[hb * kRow];
     part[g][dg] = c;
     __syncthreads();
+    if (prefix) {  // each group rewrites its own quarter: counts -> exclusive prefixes
+        uint32_t run = 0;
+        for (int gi = 0; gi < g; gi++)
+            run += part[gi][dg];
+        uint32_t hb = r0;
+        for (; hb + 4 <= r1; hb += 4) {
+            uint32_t v[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                v[k] = col[(hb + k) * kRow];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                col[(hb + k) * kRow] = run;
+                run += v[k];
+            }
+        }
+        for (; hb < r1; hb++) {
+            const uint32_t v = col[hb * kRow];
+            col[hb * kRow] = run;
+            run += v;
+        }
+    }
     if (tid >= kRadix)
         return;
     c = 0;
@@ -335,7 +376,9 @@ __device__ __forceinline__ uint64_t load_status(const uint64_t *p)
 // or done; the CTA ranks its keys in shared memory, publishes its digit
 // counts, sums the counts of the tiles before it in the same table (decoupled
 // look-back), and scatters its keys, in stable order, to the digit ranges
-// found by the histogram kernel.  A wait that runs out raises
+// found by the histogram kernel.  The first pass needs no look-back: its
+// tiles hold the keys in the order the histogram kernel counted them, and the
+// digit scan has turned those counts into each tile's offsets.  A wait that runs out raises
 // DLRM_FLAG_WAIT_TIMEOUT and writes stay inside the table's range.
 // The first pass (pass 0, which reads the indices) sorts by the top 8 row
 // bits when the MSD sort is planned and no bucket is too large (`msd_d`), by
@@ -384,7 +427,9 @@ sort_onesweep_kernel(int pass, PassDigit lsd_d, PassDigit msd_d, int role, const
         return;
     const uint32_t tau = tau_s;
     // the next pass reuses the other buffer of look-back words: clear this tile's
-    w.status[(pass + 1) & 1][(size_t)tau * kRadix + tid] = 0;
+    // (pass 1's were cleared by the histogram kernel, for every tile)
+    if (pass != 0)
+        w.status[(pass + 1) & 1][(size_t)tau * kRadix + tid] = 0;
     const uint32_t mask = (1u << nbits) - 1u;
     const int radix = 1 << nbits;
     const bool first_vals_bags = pass == 0 && *w.vals_bags != 0u;  // the first pass's values: bags or positions
@@ -453,8 +498,10 @@ sort_onesweep_kernel(int pass, PassDigit lsd_d, PassDigit msd_d, int role, const
     }
     const uint32_t t0 = w.tile_base[ti.t];  // the table's first tile
     const bool first = tau == t0;
+    // the first pass reads its tile's offsets from the digit scan; the later ones look back
+    const bool look_back = pass != 0;
     uint64_t *stat = w.status[pass & 1];
-    if (tid < radix)
+    if (look_back && tid < radix)
         store_status(stat + (size_t)tau * kRadix + tid, first ? kInclusive : kAggregate, total);
     // block-wide exclusive scan of the digit totals (radix <= 256 threads)
     uint32_t incl = total;
@@ -483,6 +530,7 @@ sort_onesweep_kernel(int pass, PassDigit lsd_d, PassDigit msd_d, int role, const
             sval[lp] = pass == 0 ? (first_vals_bags ? w.bag_of[j] : j) : vals_in[j];
         }
     }
+    // the first pass: the digit scan's prefix of this tile.  Later passes
     // look back over the tiles before this one in the table (after the local
     // scatter, so that they have had the longest time to publish): the words
     // of up to 4 tiles k, k - 1, .. (none before the table's first) are read
@@ -490,7 +538,9 @@ sort_onesweep_kernel(int pass, PassDigit lsd_d, PassDigit msd_d, int role, const
     // written is read again, with those before it
     if (tid < radix) {
         uint32_t excl = 0;
-        if (!first) {
+        if (!look_back) {
+            excl = w.tile_hist[((size_t)tau * kSortRows + crow) * kRadix + tid];
+        } else if (!first) {
             uint32_t k = tau - 1;
             int spins = 0;
             for (;;) {
@@ -977,7 +1027,9 @@ int launch_coalesce(const TableSet &ts, int T, int d, const int64_t *offsets, co
     if ((s = launch_status()) != DLRM_OK)
         return s;
     const int rows = passes + (msd ? 1 : 0);  // the MSD digit's counts are row `passes`
-    sort_digit_scan_kernel<<<(unsigned)(rows * T), kScanGroups * kRadix, 0, st>>>(msd ? passes : -1, T, w);
+    const unsigned prefix_rows = 1u | (msd ? 1u << passes : 0u);  // the rows the first pass may sort by
+    sort_digit_scan_kernel<<<(unsigned)(rows * T), kScanGroups * kRadix, 0, st>>>(msd ? passes : -1, prefix_rows,
+                                                                                   T, w);
     count_launch(st);
     if ((s = launch_status()) != DLRM_OK)
         return s;

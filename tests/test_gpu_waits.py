@@ -2,9 +2,9 @@
 limit, reports it, and writes nothing it should not (no fault, no hang).
 
 The waits are made to run out through the library's testing hook
-(dlrm_set_wait_test_hooks), never by a fault: the radix sort's tile counter
-starts past the first tile, so the next tile waits for counts that nobody
-publishes; the bulk-copy interaction kernel's stage-barrier waits are given
+(dlrm_set_wait_test_hooks), never by a fault: the radix sort's tile counters
+start past the first tile, so in the second pass (the first takes its offsets
+from the digit scan) the next tile waits for counts that nobody publishes; the bulk-copy interaction kernel's stage-barrier waits are given
 no polls at all, so each CTA gives up before its first chunk and drains its
 copies before leaving.  After each case the hooks are reset and the same
 call must again match the oracle.
@@ -56,25 +56,16 @@ def _guards_intact(buf, nbytes):
     return bool((b[:GUARD] == 0xA5).all() and (b[GUARD + nbytes:] == 0xA5).all())
 
 
-SORT_WAIT_CASES = {
-    # one table with four sort tiles, sorted by LSD passes
-    "lsd": (dict(T=1, rows=[50000], B=400, bag=("fixed", 32)), False),
-    # 18-bit rows and 256 keys per top-digit bucket: the top-digit pass waits, and the bucket
-    # sort and the LSD passes after it must leave everything alone
-    "bucket": (dict(T=1, rows=[200000], B=2048, bag=("fixed", 32)), True),
-}
-
-
-@pytest.mark.parametrize("plan", sorted(SORT_WAIT_CASES))
-def test_sort_lookback_wait_runs_out_and_nothing_is_updated(plan):
-    # the passes start claiming at tile 1, so tile 1 waits for tile 0's digit
+def test_sort_lookback_wait_runs_out_and_nothing_is_updated():
+    # one table with four sort tiles and two LSD passes; the passes start
+    # claiming at tile 1, so in the second pass (the first reads its offsets
+    # from the digit scan and never waits) tile 1 waits for tile 0's digit
     # counts, which never come
-    over, msd = SORT_WAIT_CASES[plan]
-    cfg = W.make_config("capacity", **over)
+    cfg = W.make_config("capacity", T=1, rows=[50000], B=400, bag=("fixed", 32))
     host = W.tables_host(cfg)
     offsets, indices = W.make_indices(cfg)
     assert indices.size > 3 * 4096
-    assert sdi.dlrm_emb_bag_sort_plan(cfg["rows"], indices.size)[1] == msd
+    assert sdi.dlrm_emb_bag_sort_plan(cfg["rows"], indices.size) == (2, False)
     dp = W.make_dpooled(cfg)
     nbytes = sdi.dlrm_emb_bag_bwd_workspace_size(1, cfg["B"], indices.size, cfg["d"])
     buf, ws = _guarded_workspace(nbytes)
