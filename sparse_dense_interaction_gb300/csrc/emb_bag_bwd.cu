@@ -285,10 +285,14 @@ sort_digit_scan_kernel(int msd_row, unsigned prefix_rows, int T, BwdPtrs w)
         r0 = h0 + min((uint32_t)g * q, n);
         r1 = h0 + min((uint32_t)(g + 1) * q, n);
         uint32_t hb = r0;
-        for (; hb + 4 <= r1; hb += 4) {
-            const uint32_t a0 = col[hb * kRow], a1 = col[(hb + 1) * kRow];
-            const uint32_t a2 = col[(hb + 2) * kRow], a3 = col[(hb + 3) * kRow];
-            c += (a0 + a1) + (a2 + a3);
+        for (; hb + 8 <= r1; hb += 8) {
+            uint32_t a[8];
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                a[k] = col[(hb + k) * kRow];
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                c += a[k];
         }
         for (; hb < r1; hb++)
             c += col[hb * kRow];
@@ -309,13 +313,13 @@ sort_digit_scan_kernel(int msd_row, unsigned prefix_rows, int T, BwdPtrs w)
         for (int gi = 0; gi < g; gi++)
             run += part[gi][dg];
         uint32_t hb = r0;
-        for (; hb + 4 <= r1; hb += 4) {
-            uint32_t v[4];
+        for (; hb + 8 <= r1; hb += 8) {
+            uint32_t v[8];
 #pragma unroll
-            for (int k = 0; k < 4; k++)
+            for (int k = 0; k < 8; k++)
                 v[k] = col[(hb + k) * kRow];
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
+            for (int k = 0; k < 8; k++) {
                 col[(hb + k) * kRow] = run;
                 run += v[k];
             }
