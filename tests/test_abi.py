@@ -219,3 +219,25 @@ def test_noalloc_returns_the_workspace_calls_statuses(lib):
         assert want != _native.OK, kw
         assert got == want, (kw, got, want)
     assert lib.dlrm_kernel_launch_count() == 0
+
+
+def test_sort_plan_follows_the_row_bits_and_the_bucket_sizes(lib):
+    # LSD passes: ceil(bits / 8) over the largest table's row bits
+    assert sdi.dlrm_emb_bag_sort_plan([1000], 100) == (2, False)
+    assert sdi.dlrm_emb_bag_sort_plan([256], 100) == (1, False)
+    assert sdi.dlrm_emb_bag_sort_plan([257], 100) == (2, False)
+    assert sdi.dlrm_emb_bag_sort_plan([4_000_000] * 26, 34_077_138) == (3, False)  # 5.1k keys per bucket
+    # the bucket sort: 17+ row bits, every table above half the largest power of two,
+    # 256 .. 2560 keys per (table, top digit) bucket on average
+    assert sdi.dlrm_emb_bag_sort_plan([32_000_000] * 8, 16384 * 32 * 8) == (4, True)
+    assert sdi.dlrm_emb_bag_sort_plan([1 << 16] * 2, 2 * 256 * 1000) == (2, False)  # 16 bits
+    assert sdi.dlrm_emb_bag_sort_plan([(1 << 16) + 1] * 2, 2 * 256 * 1000) == (3, True)
+    assert sdi.dlrm_emb_bag_sort_plan([200000], 256 * 256) == (3, True)
+    assert sdi.dlrm_emb_bag_sort_plan([200000], 256 * 256 - 1) == (3, False)
+    assert sdi.dlrm_emb_bag_sort_plan([200000], 256 * 2560) == (3, True)
+    assert sdi.dlrm_emb_bag_sort_plan([200000], 256 * 2560 + 1) == (3, False)
+    assert sdi.dlrm_emb_bag_sort_plan([200000, 131072], 2 * 256 * 1000) == (3, False)  # a table of 2^17 rows
+    assert sdi.dlrm_emb_bag_sort_plan([200000, 131073], 2 * 256 * 1000) == (3, True)
+    for bad in (([], 10), ([0], 10), ([100], -1)):
+        with pytest.raises(sdi.DlrmError):
+            sdi.dlrm_emb_bag_sort_plan(*bad)
